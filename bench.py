@@ -1,0 +1,416 @@
+"""Benchmark of the fused dequantise-and-multiply on GB300.
+
+Headline workload (one "step"): the 40 decoder Linears of a whisper-large-v3-turbo-shaped
+model (4 layers x {self q,k,v,o; cross q,k,v,o; fc1 1280->5120; fc2 5120->1280}), NF4 with
+double-quantised absmax, bf16 activations, one pass at each of M = 1, 4 and 16 rows:
+120 fused dequant-matmul launches.  Weights are packed once (load time) and stay resident;
+every step reads a different weight copy (9 copies, 487 MB > 3x the 129 MB L2), so each
+step streams its weights from HBM.  Metric: algorithmic GB/s (packed weights + scales + x +
+y + bias bytes per step / device time).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+
+N > 1 runs one process per GPU (torchrun), each an independent replica of the workload
+(weak scaling); the time is the max over ranks.  --impl reference times the CPU oracle
+(the plain numpy implementation the tests check against) on a bounded sample of the same
+workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), \
+        int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except Exception:
+        return None
+
+
+def peak_hbm(peaks):
+    if peaks:
+        for k in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if k in peaks and peaks[k]:
+                return float(peaks[k]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def peak_tflops(peaks, sustained):
+    if peaks:
+        keys = ("bf16_tflops_sustained",) if sustained else ("bf16_tflops",)
+        for k in keys + ("bf16_tflops",):
+            if k in peaks and peaks[k]:
+                return float(peaks[k]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+def nf4_linear_bytes(N, K, M, has_bias):
+    w = N * K // 2 + N * K // 64 + 4 * ((N * K // 64 + 255) // 256) + 4
+    return w + M * K * 2 + M * N * 2 + (N * 2 if has_bias else 0)
+
+
+def decoder_workload():
+    from bit_weight_quantized_matmul_gb300 import workloads as wl
+    return wl.turbo_decoder_sweep(), (1, 4, 16)
+
+
+def step_bytes(linears, Ms):
+    return sum(nf4_linear_bytes(l["N"], l["K"], M, l["bias"]) for M in Ms for l in linears)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, local_rank, world):
+    import torch
+    import torch.distributed as dist
+    from bit_weight_quantized_matmul_gb300 import build as B
+    B.build()
+    from bit_weight_quantized_matmul_gb300 import wq
+    from bit_weight_quantized_matmul_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    linears, Ms = decoder_workload()
+    R = 9  # weight copies: 9 x 54 MB > 3 x L2
+    # pack once from the seeded generator, then clone to R resident copies
+    packed0 = []
+    for l in linears:
+        W = torch.from_numpy(wl.weight(l["seed"], l["N"], l["K"])).to(dev)
+        packed0.append(wq.pack("nf4", W))
+        del W
+    copies = [packed0] + [[(p.clone(), s.clone()) for p, s in packed0] for _ in range(R - 1)]
+    biases = [wl.bias(l["seed"], l["N"]).to(dev) if l["bias"] else None for l in linears]
+    xs = {M: [wl.activations(l["seed"] * 7 + M, M, l["K"]).to(dev) for l in linears] for M in Ms}
+    ys = {M: [torch.empty((M, l["N"]), dtype=torch.bfloat16, device=dev) for l in linears] for M in Ms}
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def one_pass(copy, M):
+        for i, l in enumerate(linears):
+            p, s = copies[copy][i]
+            wq.linear_into(ys[M][i], xs[M][i], p, s, "nf4", l["N"], l["K"], biases[i], weights_static=True)
+
+    # eager warm-up of every path once (sets kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for M in Ms:
+            one_pass(0, M)
+    torch.cuda.synchronize()
+
+    graphs = []
+    for j in range(3):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for mi, M in enumerate(Ms):
+                one_pass((3 * j + mi) % R, M)
+        graphs.append(g)
+    launches_per_step = len(linears) * len(Ms)
+    bytes_per_step = step_bytes(linears, Ms)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for w in range(args.warmup):
+        graphs[w % 3].replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for k in range(args.steps):
+            graphs[k % 3].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms = float(t.item())
+    ms_per_step = t_ms / args.steps
+    value = world * bytes_per_step * args.steps / (t_ms * 1e-3) / 1e9  # GB/s, all ranks
+
+    # ---- end to end through the public API: pinned host x in, y out, every step
+    xh = {M: [x.cpu().pin_memory() for x in xs[M]] for M in Ms}
+    yh = {M: [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys[M]] for M in Ms}
+    h2d = sum(x.numel() * 2 for M in Ms for x in xs[M])
+    d2h = sum(y.numel() * 2 for M in Ms for y in ys[M])
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step(k):
+        with torch.cuda.stream(stream):
+            for M in Ms:
+                for i in range(len(linears)):
+                    xs[M][i].copy_(xh[M][i], non_blocking=True)
+            graphs[k % 3].replay()
+            for M in Ms:
+                for i in range(len(linears)):
+                    yh[M][i].copy_(ys[M][i], non_blocking=True)
+        stream.synchronize()
+
+    for k in range(2):
+        e2e_step(k)
+    barrier()
+    t0 = time.perf_counter()
+    for k in range(e2e_steps):
+        e2e_step(k)
+    t_e2e = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([t_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_e2e = float(t.item())
+    e2e_value = world * bytes_per_step * e2e_steps / t_e2e / 1e9
+
+    peaks = read_peaks()
+    pk, pk_src = peak_hbm(peaks)
+    achieved = bytes_per_step / (ms_per_step * 1e-3) / 1e9  # per GPU; same kernel throughout the region
+    traffic = load_traffic("wq_tc_kernel", "decoder_nf4")
+    out = {
+        "metric": "4-bit dequant-linear effective HBM bandwidth, decode (M<=16)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nf4 weights, bf16 activations, fp32 accumulate",
+        "data": "synthetic (seeded counter-based generator; random-init weights of the model's shapes)",
+        "config": {"workload": "whisper-large-v3-turbo decoder sweep: 4 layers x 10 NF4 Linears "
+                               "(1280x1280 x8, 5120x1280, 1280x5120), M in {1,4,16} -> 120 launches/step",
+                   "fmt": "nf4 block 64, double-quant absmax (int8 per 256, fp32 scale)",
+                   "l2": "inputs larger than L2: 9 rotated weight copies (487 MB)",
+                   "bytes_per_step": bytes_per_step, "launch": "CUDA graph per step, programmatic dependent launch",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk, "unit": "GB/s",
+                     "frac": round(achieved / pk, 4), "peak_source": pk_src, "traffic": traffic,
+                     "kernel": "wq_tc_kernel<16,12,NF4> (decode, cluster split-K)",
+                     "algorithmic_bytes_per_launch": round(bytes_per_step / launches_per_step, 1)},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "note": "pinned host x -> device, the step's 120 launches, y -> pinned host, synchronised"},
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0 and not args.no_extra:
+        out["extra"] = extra_gemm(wq, wl, dev, peaks)
+    return out
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, when it matches the current kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(workload, {}).get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def extra_gemm(wq, wl, dev, peaks):
+    """Encoder-side context: NVFP4 W4A16 fc1 GEMM at M = 1500 x 4 (TFLOPS, L2-cold weights)."""
+    import torch
+    M, N, K = 6000, 5120, 1280
+    W = torch.from_numpy(wl.weight(101, N, K)).to(dev)
+    p, s = wq.pack("nvfp4", W)
+    x = wl.activations(101, M, K, outlier_frac=0.001).to(dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        wq.linear_into(y, x, p, s, "nvfp4", N, K)
+    times = []
+    for _ in range(10):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        wq.linear_into(y, x, p, s, "nvfp4", N, K)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    t = statistics.median(times)
+    tflops = 2.0 * M * N * K / (t * 1e-3) / 1e12
+    pk, src = peak_tflops(peaks, sustained=False)
+    return {"workload": "encoder fc1 NVFP4 W4A16, M=6000 N=5120 K=1280 (B=4 windows)",
+            "value": round(tflops, 1), "unit": "TFLOP/s", "ms": round(t, 4),
+            "roofline": {"bound": "tensor", "peak": pk, "peak_source": src, "frac": round(tflops / pk, 4)}}
+
+
+# ---------------------------------------------------------------- CPU oracle
+_ORACLE_CACHE = {}
+
+
+def _oracle_inputs():
+    """Oracle-packed weights and fp32 inputs of the decoder sweep (built once, not timed)."""
+    if "items" not in _ORACLE_CACHE:
+        from bit_weight_quantized_matmul_gb300 import workloads as wl
+        from oracle import quant as Q
+        linears, Ms = decoder_workload()
+        items = []
+        for l in linears:
+            p = Q.nf4_pack(wl.weight(l["seed"], l["N"], l["K"]))
+            b = wl.bf16_as_f32(wl.bias(l["seed"], l["N"])) if l["bias"] else None
+            for M in Ms:
+                x = wl.bf16_as_f32(wl.activations(l["seed"] * 7 + M, M, l["K"]))
+                items.append((l, M, p, x, b))
+        _ORACLE_CACHE["items"] = items
+    return _ORACLE_CACHE["items"]
+
+
+def cpu_baseline(seconds=15.0):
+    """The oracle (numpy NF4 decode + fp64 matmul, as it stands) on a bounded sample of the
+    same workload: whole passes over the step's 120 Linear-calls, repeated until ``seconds``
+    of CPU work (a partial pass at the end counts the Linears it finished)."""
+    from oracle import linear as L
+    items = _oracle_inputs()
+    done_bytes, t_total, n = 0, 0.0, 0
+    while t_total < seconds:
+        for l, M, p, x, b in items:
+            t0 = time.perf_counter()
+            L.linear_w4a16(x, p, b)
+            t_total += time.perf_counter() - t0
+            done_bytes += nf4_linear_bytes(l["N"], l["K"], M, l["bias"])
+            n += 1
+            if t_total >= seconds:
+                break
+    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} Linear-calls of the step's 120 (whole passes in order), numpy NF4 decode + "
+                      f"fp64 matmul, {t_total:.1f} s of CPU time",
+            "threads_note": "numpy elementwise single-threaded; fp64 matmul on the BLAS thread pool"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, on the same config and metric; each step a bounded
+    time-sliced sample so that warm-up + steps take about two minutes."""
+    if rank != 0:
+        return None
+    _oracle_inputs()
+    per = max(0.2, min(args.ref_step_seconds, 120.0 / (args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(seconds=per)
+    t0 = time.perf_counter()
+    vals = [cpu_baseline(seconds=per)["value"] for _ in range(args.steps)]
+    elapsed = time.perf_counter() - t0
+    v = statistics.median(vals)
+    return {"impl": "reference", "metric": "4-bit dequant-linear effective HBM bandwidth, decode (M<=16)",
+            "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1000 * elapsed / max(1, args.steps), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp32 decode, fp64 matmul",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": "whisper-large-v3-turbo decoder sweep: 4 layers x 10 NF4 Linears, "
+                                   "M in {1,4,16}; each step a bounded sample of it"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{per:.2f} s of oracle work per step over the step's Linear-calls"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=5.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    out = run_ours(args, rank, local_rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

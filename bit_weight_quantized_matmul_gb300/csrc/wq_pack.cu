@@ -1,0 +1,437 @@
+// wq_pack.cu -- GPU packers, the decode-to-fp32 export and the NVFP4 runtime
+// activation quantiser.  Every quantiser step is one IEEE fp32 operation
+// (__fdiv_rn / __fmul_rn / __fadd_rn / __fsub_rn, rintf = round half to even),
+// so the bytes are identical to a plain sequential evaluation of the block
+// definitions.
+//
+// Sources: PR "asr: add a 4-bit nf4 option for the Whisper engine", "What's
+// here" (NF4 + double-quant); model card "whisper-large-v3-turbo -- NVFP4",
+// "What is quantized" (E2M1 per 16, E4M3 block scale, fp32 global scale,
+// runtime activation quantisation); PR "Run quantized Whisper on the fused
+// Metal decode path", "Summary" (q4_0 / q8_0 blocks of 32 with an fp16 d).
+#include <cuda_runtime.h>
+
+#include "wq_device.cuh"
+#include "wq_internal.h"
+
+namespace wq {
+namespace {
+
+constexpr int kNF4Block = 64;
+constexpr int kDQGroup = 256;
+constexpr int kNVBlock = 16;
+constexpr int kGGBlock = 32;
+
+inline int grid_for(int64_t n, int threads) {
+  int64_t g = (n + threads - 1) / threads;
+  return (int)(g < 1 ? 1 : g);
+}
+
+// ------------------------------------------------------------------ NF4
+// 1) per 64-block absmax -> fp32, parked in the (not yet written) packed buffer.
+__global__ void nf4_absmax_kernel(const float* __restrict__ W, int64_t nb, float* __restrict__ tmp) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nb) return;
+  const float4* src = reinterpret_cast<const float4*>(W + b * kNF4Block);
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kNF4Block / 4; ++i) {
+    const float4 v = src[i];
+    a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  tmp[b] = a;
+}
+
+// Exact sum of non-negative fp32 values kept as per-exponent integer mantissa
+// sums, converted once to fp64 with round-to-nearest-even.
+// total = sum_e bucket[e] * 2^(e - 150), e = biased exponent (subnormals use e = 1).
+__device__ double exact_bucket_sum_to_double(const unsigned long long* bucket) {
+  unsigned long long L[7] = {0, 0, 0, 0, 0, 0, 0};  // B = total * 2^149, 448 bits
+  for (int e = 1; e < 255; ++e) {
+    const unsigned long long v = bucket[e];
+    if (!v) continue;
+    const int sh = e - 1, li = sh >> 6, bi = sh & 63;
+    const unsigned long long lo = v << bi;
+    const unsigned long long hi = bi ? (v >> (64 - bi)) : 0ull;
+    unsigned long long old = L[li];
+    L[li] += lo;
+    unsigned long long add = hi + (L[li] < old ? 1ull : 0ull);
+    for (int j = li + 1; add && j < 7; ++j) {
+      old = L[j];
+      L[j] += add;
+      add = (L[j] < old) ? 1ull : 0ull;
+    }
+  }
+  int top = -1;
+  for (int i = 6; i >= 0; --i)
+    if (L[i]) { top = i * 64 + 63 - __clzll((long long)L[i]); break; }
+  if (top < 0) return 0.0;
+  if (top <= 52) return ldexp((double)L[0], -149);
+  int sh = top - 52;  // keep bits [sh, top]
+  const int li = sh >> 6, bi = sh & 63;
+  unsigned long long mant = L[li] >> bi;
+  if (bi && li + 1 < 7) mant |= L[li + 1] << (64 - bi);
+  mant &= (1ull << 53) - 1;
+  const int rp = sh - 1;  // rounding bit position
+  const unsigned long long rnd = (L[rp >> 6] >> (rp & 63)) & 1ull;
+  bool sticky = (L[rp >> 6] & ((1ull << (rp & 63)) - 1ull)) != 0ull;
+  for (int i = 0; i < (rp >> 6); ++i) sticky = sticky || (L[i] != 0ull);
+  if (rnd && (sticky || (mant & 1ull))) {
+    ++mant;
+    if (mant >> 53) { mant >>= 1; ++sh; }
+  }
+  return ldexp((double)mant, sh - 149);
+}
+
+// 2) one CTA: offset = fp32(exact_sum(absmax) / count); per group of 256:
+//    t = a - offset, s2 = max|t| / 127, q = clamp(rint(t / s2), -127, 127).
+__global__ void __launch_bounds__(1024) nf4_double_quant_kernel(const float* __restrict__ tmp, int64_t nb,
+                                                                int8_t* __restrict__ absmax_q,
+                                                                float* __restrict__ s2_out,
+                                                                float* __restrict__ offset_out,
+                                                                int64_t pad_end) {
+  __shared__ unsigned long long bucket[256];
+  __shared__ float s_offset;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 256; i += blockDim.x) bucket[i] = 0ull;
+  __syncthreads();
+  for (int64_t base = 0; base < nb; base += blockDim.x) {
+    const int64_t i = base + tid;
+    uint32_t e = 1, m = 0;
+    if (i < nb) {
+      const uint32_t bits = __float_as_uint(tmp[i]);
+      e = bits >> 23;
+      m = bits & 0x7FFFFFu;
+      if (e) m |= 0x800000u; else e = 1;
+    }
+    const unsigned mask = __match_any_sync(0xFFFFFFFFu, e);
+    const unsigned sum = __reduce_add_sync(mask, m);  // <= 32 * 2^24 fits 32 bits
+    if ((int)(tid & 31) == __ffs(mask) - 1 && sum) atomicAdd(&bucket[e], (unsigned long long)sum);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const double total = exact_bucket_sum_to_double(bucket);
+    const float off = __double2float_rn(__ddiv_rn(total, (double)nb));
+    s_offset = off;
+    *offset_out = off;
+    for (int64_t p = nb; p < pad_end; ++p) absmax_q[p] = 0;
+  }
+  __syncthreads();
+  const float off = s_offset;
+  const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  const int64_t ng = (nb + kDQGroup - 1) / kDQGroup;
+  for (int64_t g = warp; g < ng; g += nwarps) {
+    float t[kDQGroup / 32];
+    uint32_t mx = 0;
+#pragma unroll
+    for (int j = 0; j < kDQGroup / 32; ++j) {
+      const int64_t i = g * kDQGroup + j * 32 + lane;
+      t[j] = (i < nb) ? __fsub_rn(tmp[i], off) : 0.0f;
+      const uint32_t ab = __float_as_uint(fabsf(t[j]));
+      mx = (i < nb && ab > mx) ? ab : mx;
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    const float s2 = __fdiv_rn(__uint_as_float(mx), 127.0f);
+    if (lane == 0) s2_out[g] = s2;
+#pragma unroll
+    for (int j = 0; j < kDQGroup / 32; ++j) {
+      const int64_t i = g * kDQGroup + j * 32 + lane;
+      if (i < nb) {
+        float q = 0.0f;
+        if (s2 != 0.0f) q = fminf(fmaxf(rintf(__fdiv_rn(t[j], s2)), -127.0f), 127.0f);
+        absmax_q[i] = (int8_t)(int)q;
+      }
+    }
+  }
+}
+
+// 3) codes: v = w / absmax (0 for an all-zero block); code = #{midpoints < v}.
+__global__ void nf4_codes_kernel(const float* __restrict__ W, int64_t nb, uint8_t* __restrict__ packed) {
+  __shared__ float mids[15];
+  if (threadIdx.x < 15)
+    mids[threadIdx.x] = __fmul_rn(__fadd_rn(kNF4[threadIdx.x], kNF4[threadIdx.x + 1]), 0.5f);
+  __syncthreads();
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nb) return;
+  const float4* src = reinterpret_cast<const float4*>(W + b * kNF4Block);
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kNF4Block / 4; ++i) {
+    const float4 v = src[i];
+    a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  uint4* dst = reinterpret_cast<uint4*>(packed + b * (kNF4Block / 2));
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {  // 32 elements -> 16 bytes per store
+    uint32_t word[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t acc = 0;
+      const float4 v0 = src[q * 8 + w * 2], v1 = src[q * 8 + w * 2 + 1];
+      const float vals[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float v = (a == 0.0f) ? 0.0f : __fdiv_rn(vals[j], a);
+        uint32_t code = 0;
+#pragma unroll
+        for (int k = 0; k < 15; ++k) code += (mids[k] < v) ? 1u : 0u;
+        acc |= code << (4 * j);
+      }
+      word[w] = acc;
+    }
+    dst[q] = make_uint4(word[0], word[1], word[2], word[3]);
+  }
+}
+
+// ------------------------------------------------------------------ NVFP4
+template <typename T>
+__device__ __forceinline__ float load_as_f32(const T* p, int64_t i);
+template <>
+__device__ __forceinline__ float load_as_f32<float>(const float* p, int64_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float load_as_f32<uint16_t>(const uint16_t* p, int64_t i) {
+  return bf16_bits_to_f32(p[i]);
+}
+
+// amax over n values -> atomicMax on the bit pattern (non-negative floats order as integers)
+template <typename T>
+__global__ void amax_kernel(const T* __restrict__ X, int64_t n, unsigned* __restrict__ slot) {
+  float a = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    a = fmaxf(a, fabsf(load_as_f32(X, i)));
+  unsigned u = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(a));
+  if ((threadIdx.x & 31) == 0 && u) atomicMax(slot, u);
+}
+
+__device__ __forceinline__ float nvfp4_g_from_amax(float amax) {
+  return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+}
+
+// one thread per 16-block along a row: s = e4m3((amax_b / 6) / g), S = dec(s) * g,
+// code = e2m1(x / S) (0 where S == 0).  g_src holds amax (g_is_amax) or g itself.
+template <typename T>
+__global__ void nvfp4_quant_kernel(const T* __restrict__ X, int64_t nblk, const float* __restrict__ g_src,
+                                   int g_is_amax, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                   float* __restrict__ g_copy_out) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const float gs = *g_src;
+  const float g = g_is_amax ? nvfp4_g_from_amax(gs) : gs;
+  if (b == 0 && g_copy_out) *g_copy_out = g;
+  if (b >= nblk) return;
+  float v[kNVBlock];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kNVBlock; ++i) {
+    v[i] = load_as_f32(X, b * kNVBlock + i);
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const uint32_t s = f32_to_e4m3_satfinite(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
+  const float S = __fmul_rn(e4m3_to_f32(s), g);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < kNVBlock; ++i) {
+    const uint32_t c = (S == 0.0f) ? 0u : f32_to_e2m1(__fdiv_rn(v[i], S));
+    if (i < 8) lo |= c << (4 * i); else hi |= c << (4 * (i - 8));
+  }
+  reinterpret_cast<uint2*>(codes)[b] = make_uint2(lo, hi);
+  sf[b] = (uint8_t)s;
+}
+
+// slot: amax -> g; zero the pad bytes between the block scales and g.
+__global__ void nvfp4_finalize_kernel(float* slot, uint8_t* pad_begin, int pad_len) {
+  if (threadIdx.x == 0) *slot = nvfp4_g_from_amax(*slot);
+  if ((int)threadIdx.x < pad_len) pad_begin[threadIdx.x] = 0;
+}
+
+// ------------------------------------------------------------------ q4_0 / q8_0
+__global__ void q4_0_kernel(const float* __restrict__ W, int64_t nb, uint8_t* __restrict__ packed,
+                            uint16_t* __restrict__ d_out) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nb) return;
+  const float4* src = reinterpret_cast<const float4*>(W + b * kGGBlock);
+  float v[kGGBlock];
+#pragma unroll
+  for (int i = 0; i < kGGBlock / 4; ++i) {
+    const float4 t = src[i];
+    v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+  }
+  float best = -1.0f, ext = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kGGBlock; ++i)
+    if (fabsf(v[i]) > best) { best = fabsf(v[i]); ext = v[i]; }  // strict: first index wins ties
+  const __half d16 = __float2half_rn(__fdiv_rn(ext, -8.0f));
+  const float d = __half2float(d16);
+  uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < kGGBlock; ++i) {
+    float q = 8.0f;
+    if (d != 0.0f) q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(v[i], d)), 8.0f), 0.0f), 15.0f);
+    w[i >> 3] |= ((uint32_t)q) << (4 * (i & 7));
+  }
+  reinterpret_cast<uint4*>(packed)[b] = make_uint4(w[0], w[1], w[2], w[3]);
+  d_out[b] = __half_as_ushort(d16);
+}
+
+__global__ void q8_0_kernel(const float* __restrict__ W, int64_t nb, int8_t* __restrict__ packed,
+                            uint16_t* __restrict__ d_out) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nb) return;
+  const float4* src = reinterpret_cast<const float4*>(W + b * kGGBlock);
+  float v[kGGBlock];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kGGBlock / 4; ++i) {
+    const float4 t = src[i];
+    v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(t.x), fabsf(t.y)), fmaxf(fabsf(t.z), fabsf(t.w))));
+  }
+  const __half d16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
+  const float d = __half2float(d16);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = 0;
+#pragma unroll
+  for (int i = 0; i < kGGBlock; ++i) {
+    float q = 0.0f;
+    if (d != 0.0f) q = fminf(fmaxf(rintf(__fdiv_rn(v[i], d)), -127.0f), 127.0f);
+    w[i >> 2] |= ((uint32_t)(uint8_t)(int8_t)(int)q) << (8 * (i & 3));
+  }
+  uint4* dst = reinterpret_cast<uint4*>(packed + b * kGGBlock);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  d_out[b] = __half_as_ushort(d16);
+}
+
+// ------------------------------------------------------------------ dequant export
+// one thread per 8 consecutive elements
+__global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales, int fmt,
+                               int64_t n8, ScalesLayout lay, float* __restrict__ out) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n8) return;
+  const int64_t e0 = t * 8;
+  float r[8];
+  if (fmt == WQ_Q8_0) {
+    const uint2 c = reinterpret_cast<const uint2*>(packed)[t];
+    const float d = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(scales)[e0 / kGGBlock]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int8_t q = (int8_t)(((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFF);
+      r[j] = __fmul_rn((float)q, d);
+    }
+  } else {
+    const uint32_t c = reinterpret_cast<const uint32_t*>(packed)[t];
+    if (fmt == WQ_NF4) {
+      const int64_t b = e0 / kNF4Block;
+      const int8_t q = reinterpret_cast<const int8_t*>(scales)[b];
+      const float s2 = reinterpret_cast<const float*>(scales + lay.s2_off)[b / kDQGroup];
+      const float off = *reinterpret_cast<const float*>(scales + lay.offset_off);
+      const float a = __fadd_rn(__fmul_rn((float)q, s2), off);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) r[j] = __fmul_rn(kNF4[(c >> (4 * j)) & 15u], a);
+    } else if (fmt == WQ_NVFP4 || fmt == WQ_NVFP4_W4A4) {
+      const float s = e4m3_to_f32(scales[e0 / kNVBlock]);
+      const float g = *reinterpret_cast<const float*>(scales + lay.g_off);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) r[j] = __fmul_rn(__fmul_rn(kE2M1[(c >> (4 * j)) & 15u], s), g);
+    } else {  // q4_0
+      const float d = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(scales)[e0 / kGGBlock]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) r[j] = __fmul_rn((float)((int)((c >> (4 * j)) & 15u) - 8), d);
+    }
+  }
+  float4* o = reinterpret_cast<float4*>(out + e0);
+  o[0] = make_float4(r[0], r[1], r[2], r[3]);
+  o[1] = make_float4(r[4], r[5], r[6], r[7]);
+}
+
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host entry points
+int pack_nf4(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s) {
+  const int64_t nb = N * K / kNF4Block;
+  if (nb == 0) return WQ_OK;
+  const ScalesLayout lay = scales_layout(WQ_NF4, N, K);
+  float* tmp = reinterpret_cast<float*>(packed);  // 4 * nb <= N*K/2 bytes: scratch inside the output
+  nf4_absmax_kernel<<<grid_for(nb, 256), 256, 0, s>>>(W, nb, tmp);
+  nf4_double_quant_kernel<<<1, 1024, 0, s>>>(tmp, nb, reinterpret_cast<int8_t*>(scales),
+                                             reinterpret_cast<float*>(scales + lay.s2_off),
+                                             reinterpret_cast<float*>(scales + lay.offset_off),
+                                             (int64_t)lay.s2_off);
+  nf4_codes_kernel<<<grid_for(nb, 128), 128, 0, s>>>(W, nb, packed);
+  count_launch(3);
+  return launch_status();
+}
+
+int pack_nvfp4(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s) {
+  const int64_t n = N * K, nblk = n / kNVBlock;
+  if (n == 0) return WQ_OK;
+  const ScalesLayout lay = scales_layout(WQ_NVFP4, N, K);
+  float* slot = reinterpret_cast<float*>(scales + lay.g_off);
+  if (cudaMemsetAsync(slot, 0, sizeof(float), s) != cudaSuccess) return WQ_ERR_CUDA;
+  int g = grid_for(n, 256);
+  if (g > 4096) g = 4096;
+  amax_kernel<float><<<g, 256, 0, s>>>(W, n, reinterpret_cast<unsigned*>(slot));
+  nvfp4_quant_kernel<float><<<grid_for(nblk, 256), 256, 0, s>>>(W, nblk, slot, 1, packed, scales, nullptr);
+  nvfp4_finalize_kernel<<<1, 32, 0, s>>>(slot, scales + lay.sf_bytes, (int)(lay.g_off - lay.sf_bytes));
+  count_launch(3);
+  return launch_status();
+}
+
+int pack_q4_0(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s) {
+  const int64_t nb = N * K / kGGBlock;
+  if (nb == 0) return WQ_OK;
+  q4_0_kernel<<<grid_for(nb, 128), 128, 0, s>>>(W, nb, packed, reinterpret_cast<uint16_t*>(scales));
+  count_launch();
+  return launch_status();
+}
+
+int pack_q8_0(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s) {
+  const int64_t nb = N * K / kGGBlock;
+  if (nb == 0) return WQ_OK;
+  q8_0_kernel<<<grid_for(nb, 128), 128, 0, s>>>(W, nb, reinterpret_cast<int8_t*>(packed),
+                                                reinterpret_cast<uint16_t*>(scales));
+  count_launch();
+  return launch_status();
+}
+
+int dequant(const uint8_t* packed, const uint8_t* scales, int fmt, int64_t N, int64_t K, float* out,
+            cudaStream_t s) {
+  const int64_t n8 = N * K / 8;
+  if (n8 == 0) return WQ_OK;
+  dequant_kernel<<<grid_for(n8, 256), 256, 0, s>>>(packed, scales, fmt, n8, scales_layout(fmt, N, K), out);
+  count_launch();
+  return launch_status();
+}
+
+int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, uint8_t* codes,
+                    uint8_t* scales, float* g_out, cudaStream_t s) {
+  const int64_t n = M * K, nblk = n / kNVBlock;
+  if (n == 0) return WQ_OK;
+  if (g_in) {
+    nvfp4_quant_kernel<uint16_t><<<grid_for(nblk, 256), 256, 0, s>>>(x, nblk, g_in, 0, codes, scales, g_out);
+    count_launch();
+    return launch_status();
+  }
+  if (cudaMemsetAsync(g_out, 0, sizeof(float), s) != cudaSuccess) return WQ_ERR_CUDA;
+  int g = grid_for(n, 256);
+  if (g > 4096) g = 4096;
+  amax_kernel<uint16_t><<<g, 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(g_out));
+  nvfp4_quant_kernel<uint16_t><<<grid_for(nblk, 256), 256, 0, s>>>(x, nblk, g_out, 1, codes, scales, nullptr);
+  nvfp4_finalize_kernel<<<1, 32, 0, s>>>(g_out, nullptr, 0);
+  count_launch(3);
+  return launch_status();
+}
+
+int take_status_pack() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return WQ_ERR_CUDA;
+  cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace wq

@@ -1,0 +1,451 @@
+// wq_tc.cu -- tensor-core fused dequantise-and-multiply for bf16 activations
+// (NF4, NVFP4 W4A16, q4_0, q8_0), decode (M <= 16) and encoder-sized M alike.
+//
+// The operation (PR "asr: add a 4-bit nf4 option for the Whisper engine",
+// "Why NF4 and not the NVFP4 snapshot"): y = x . dequant(W)^T + bias without
+// ever writing the decoded W to memory -- unpacking to bf16 and calling an
+// ordinary GEMM is what made the modelopt formats 4x slower there.
+//
+// Mapping onto sm_103a (transposed product, D^T = W_hat . x^T):
+//   * MMA "A" = a 128-row tile of decoded weights.  Four dequant warps read the
+//     packed codes that TMA staged in shared memory, decode them in registers
+//     and store bf16 pairs straight into TENSOR MEMORY with tcgen05.st: the
+//     decoded weights never touch shared memory.
+//   * MMA "B" = BN rows of x, staged by TMA with the 128-byte swizzle the MMA
+//     descriptor expects.
+//   * tcgen05.mma.kind::f16 (bf16 x bf16 -> fp32) accumulates D[128 x BN] in
+//     TMEM; one elected thread issues it.
+//   * Decode (M <= 16, BN = 16) splits K over a thread-block cluster; the
+//     partial D tiles are summed through distributed shared memory.
+//   * Epilogue: tcgen05.ld, x global scale (NVFP4), + bias, bf16 (or fp32) store.
+// All mbarrier waits are bounded (see wq_device.cuh).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "wq_device.cuh"
+#include "wq_internal.h"
+
+namespace wq {
+namespace {
+
+constexpr int kKS = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16 x)
+constexpr int kRows = 128;     // weight rows per tile (the MMA M)
+constexpr int kNA = 4;         // TMEM A-operand ring slots (32 columns each)
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 dequant + epilogue
+
+struct TcParams {
+  const uint8_t* scales;
+  const uint16_t* bias;
+  void* y;
+  int M, N, K;
+  int out_f32;
+  int ksplit;            // CTAs along K (a cluster when > 1)
+  int weights_static;    // programmatic dependent launch: stream W before the dependency resolves
+  ScalesLayout lay;
+};
+
+template <int FMT>
+struct Fmt {
+  static constexpr int WB = (FMT == WQ_Q8_0) ? 64 : 32;  // packed bytes per row per stage
+};
+
+template <int BN, int STAGES, int FMT>
+struct Smem {
+  static constexpr int XB = BN * 128;                 // x stage bytes (BN rows x 64 bf16)
+  static constexpr int WB = kRows * Fmt<FMT>::WB;     // packed weight stage bytes
+  static constexpr int X_OFF = 0;
+  static constexpr int W_OFF = X_OFF + STAGES * XB;
+  static constexpr int LUT_OFF = W_OFF + STAGES * WB;  // 256 x float2
+  static constexpr int BAR_OFF = LUT_OFF + 256 * 8;
+  static constexpr int NBAR = 2 * STAGES + 2 * kNA + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tmem base, abort flag
+  static constexpr int RED_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
+  static constexpr int RED_BYTES = (BN <= 16) ? kRows * (BN + 1) * 4 : 0;
+  static constexpr int TOTAL = RED_OFF + RED_BYTES + 1024;  // + alignment slack
+};
+
+template <int BN>
+struct TmemCols {
+  static constexpr int D_COL = kNA * 32;  // D after the A ring
+  static constexpr int USED = D_COL + BN;
+  static constexpr int ALLOC = USED <= 256 ? 256 : 512;
+};
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// Byte -> (value of low nibble, value of high nibble) for the 4-bit formats.
+template <int FMT>
+__device__ __forceinline__ float nibble_value(uint32_t c) {
+  if (FMT == WQ_NF4) return kNF4[c];
+  if (FMT == WQ_Q4_0) return (float)((int)c - 8);
+  return kE2M1[c];  // NVFP4: E2M1 value; the E4M3 block scale multiplies it, g is applied on D
+}
+
+// Decode the 64 weights [k0, k0 + 64) of row n into 32 bf16x2 words.
+template <int FMT>
+__device__ __forceinline__ void decode_chunk(const TcParams& p, const uint8_t* wrow, const float2* lut, int64_t n,
+                                             int64_t k0, bool row_ok, uint32_t (&out)[32]) {
+  if (FMT == WQ_Q8_0) {
+    float d0 = 0.0f, d1 = 0.0f;
+    if (row_ok) {
+      const uint32_t dd = *reinterpret_cast<const uint32_t*>(p.scales + 2 * ((n * p.K + k0) / 32));
+      d0 = f16_bits_to_f32(dd & 0xFFFFu);
+      d1 = f16_bits_to_f32(dd >> 16);
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(wrow);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = src[q];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      const float d = (q < 2) ? d0 : d1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a0 = (float)(int8_t)(u[j] & 0xFF), a1 = (float)(int8_t)((u[j] >> 8) & 0xFF);
+        const float a2 = (float)(int8_t)((u[j] >> 16) & 0xFF), a3 = (float)(int8_t)(u[j] >> 24);
+        out[q * 8 + j * 2] = pack_bf16x2(__fmul_rn(a0, d), __fmul_rn(a1, d));
+        out[q * 8 + j * 2 + 1] = pack_bf16x2(__fmul_rn(a2, d), __fmul_rn(a3, d));
+      }
+    }
+    return;
+  }
+  // 4-bit formats: 32 bytes, element 2j in the low nibble of byte j
+  float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // scale per 16 elements of the chunk
+  if (row_ok) {
+    if (FMT == WQ_NF4) {
+      const int64_t b = (n * p.K + k0) / 64;
+      const int8_t q = reinterpret_cast<const int8_t*>(p.scales)[b];
+      const float s2 = reinterpret_cast<const float*>(p.scales + p.lay.s2_off)[b / 256];
+      const float off = *reinterpret_cast<const float*>(p.scales + p.lay.offset_off);
+      const float a = __fadd_rn(__fmul_rn((float)q, s2), off);
+      sc[0] = sc[1] = sc[2] = sc[3] = a;
+    } else if (FMT == WQ_Q4_0) {
+      const uint32_t dd = *reinterpret_cast<const uint32_t*>(p.scales + 2 * ((n * p.K + k0) / 32));
+      sc[0] = sc[1] = f16_bits_to_f32(dd & 0xFFFFu);
+      sc[2] = sc[3] = f16_bits_to_f32(dd >> 16);
+    } else {  // NVFP4
+      const uint32_t s4 = *reinterpret_cast<const uint32_t*>(p.scales + (n * p.K + k0) / 16);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[j] = e4m3_to_f32((s4 >> (8 * j)) & 0xFFu);
+    }
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(wrow);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint4 v = src[q];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int byte_idx = q * 16 + j * 4 + b;  // elements 2*byte_idx, 2*byte_idx + 1
+        const float2 lv = lut[(u[j] >> (8 * b)) & 0xFFu];
+        const float s = sc[byte_idx >> 3];
+        out[byte_idx] = pack_bf16x2(__fmul_rn(lv.x, s), __fmul_rn(lv.y, s));
+      }
+    }
+  }
+}
+
+template <int BN, int STAGES, int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    wq_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, TcParams p) {
+  using S = Smem<BN, STAGES, FMT>;
+  using T = TmemCols<BN>;
+  constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
+  constexpr uint32_t STAGE_TX = (uint32_t)(S::XB + S::WB);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* afull = bars + 2 * STAGES;
+  uint64_t* aempty = afull + kNA;
+  uint64_t* dfull = aempty + kNA;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
+  float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
+
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  const int n0 = blockIdx.x * kRows;
+  const int m0 = blockIdx.y * BN;
+  const int nchunk_total = p.K / kKS;
+  const int z = blockIdx.z;
+  const int kc_begin = (int)((int64_t)z * nchunk_total / p.ksplit);
+  const int kc_end = (int)((int64_t)(z + 1) * nchunk_total / p.ksplit);
+  const int nchunks = kc_end - kc_begin;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1 + 4); }
+    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], 4); mbar_init(&aempty[i], 1); }
+    mbar_init(dfull, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (FMT != WQ_Q8_0) {
+    for (int i = threadIdx.x; i < 256; i += kThreads)
+      lut[i] = make_float2(nibble_value<FMT>(i & 15u), nibble_value<FMT>(i >> 4));
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, T::ALLOC);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmX);
+      prefetch_tmap(&tmW);
+      const int pre = p.weights_static ? (nchunks < STAGES ? nchunks : STAGES) : 0;
+      for (int i = 0; i < pre; ++i) {  // weights first: they do not depend on the preceding kernel
+        mbar_arrive_expect_tx(&full[i], STAGE_TX);
+        tma_load_2d(smem + S::W_OFF + i * S::WB, &tmW, &full[i], (kc_begin + i) * Fmt<FMT>::WB, n0);
+      }
+      griddep_wait();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(smem + S::X_OFF + i * S::XB, &tmX, &full[i], (kc_begin + i) * kKS, m0);
+      for (int i = pre; i < nchunks; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&full[s], STAGE_TX);
+        tma_load_2d(smem + S::W_OFF + s * S::WB, &tmW, &full[s], (kc_begin + i) * Fmt<FMT>::WB, n0);
+        tma_load_2d(smem + S::X_OFF + s * S::XB, &tmX, &full[s], (kc_begin + i) * kKS, m0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t d_tmem = tmem_base + T::D_COL;
+      for (int i = 0; i < nchunks; ++i) {
+        const int s = i % STAGES, slot = i % kNA;
+        if (!mbar_wait(&full[s], (i / STAGES) & 1, abort_flag)) break;
+        if (!mbar_wait(&afull[slot], (i / kNA) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t xaddr = smem_u32(smem + S::X_OFF + s * S::XB);
+#pragma unroll
+        for (int kk = 0; kk < kKS / 16; ++kk) {
+          const uint64_t bdesc = smem_desc(xaddr + kk * 32, 16, 1024, 2);
+          mma_bf16_ts(d_tmem, tmem_base + slot * 32 + kk * 8, bdesc, IDESC, (i | kk) != 0 ? 1u : 0u);
+        }
+        tc_commit(&aempty[slot]);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(dfull);
+    }
+  } else {
+    // ---------------- dequant warps (then epilogue)
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;      // weight row within the tile
+    const int64_t n = (int64_t)n0 + r;
+    const bool row_ok = n < p.N;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    for (int i = 0; i < nchunks; ++i) {
+      const int s = i % STAGES, slot = i % kNA;
+      if (!mbar_wait(&full[s], (i / STAGES) & 1, abort_flag)) break;
+      if (i >= kNA && !mbar_wait(&aempty[slot], ((i / kNA) & 1) ^ 1, abort_flag)) break;
+      uint32_t v[32];
+      decode_chunk<FMT>(p, smem + S::W_OFF + s * S::WB + r * Fmt<FMT>::WB, lut, n,
+                        (int64_t)(kc_begin + i) * kKS, row_ok, v);
+      tmem_st32(tmem_base + lane_base + slot * 32, v);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) { mbar_arrive(&afull[slot]); mbar_arrive(&empty[s]); }
+    }
+
+    // ---------------- epilogue
+    const bool have_d = mbar_wait(dfull, 0, abort_flag);
+    tc_fence_after();
+    griddep_wait();
+    float gsc = 1.0f;
+    if (FMT == WQ_NVFP4) gsc = *reinterpret_cast<const float*>(p.scales + p.lay.g_off);
+    const float bval = (p.bias && row_ok) ? bf16_bits_to_f32(p.bias[n]) : 0.0f;
+    float* red = reinterpret_cast<float*>(smem + S::RED_OFF);
+    if (have_d) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float acc[16];
+        tmem_ld16(tmem_base + lane_base + T::D_COL + c0, acc);
+        tc_wait_ld();
+        if (p.ksplit == 1) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < p.M && row_ok) {
+              const float val = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
+              if (p.out_f32)
+                reinterpret_cast<float*>(p.y)[(int64_t)m * p.N + n] = val;
+              else
+                reinterpret_cast<__nv_bfloat16*>(p.y)[(int64_t)m * p.N + n] = __float2bfloat16_rn(val);
+            }
+          }
+        } else if (S::RED_BYTES) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) red[r * (BN + 1) + c0 + j] = acc[j];
+        }
+      }
+    } else if (p.ksplit > 1 && S::RED_BYTES) {
+      for (int j = 0; j < BN; ++j) red[r * (BN + 1) + j] = 0.0f;
+    }
+  }
+
+  // ---------------- split-K: sum the cluster's partial tiles through DSMEM
+  if (S::RED_BYTES && p.ksplit > 1) {
+    __syncwarp();
+    cluster_sync();
+    if (warp >= 2) {
+      const int ks = p.ksplit;
+      const uint32_t rank = cluster_ctarank();
+      const int r_lo = (int)(rank * kRows / ks), r_hi = (int)((rank + 1) * kRows / ks);
+      const int rows = r_hi - r_lo;
+      const int mcount = (p.M - m0) < BN ? (p.M - m0) : BN;
+      float gsc = 1.0f;
+      if (FMT == WQ_NVFP4) gsc = *reinterpret_cast<const float*>(p.scales + p.lay.g_off);
+      const uint32_t red_base = smem_u32(smem + S::RED_OFF);
+      for (int idx = (int)threadIdx.x - 64; idx < rows * mcount; idx += 128) {
+        const int j = idx / rows, rr = r_lo + idx % rows;
+        const int64_t n = (int64_t)n0 + rr;
+        if (n >= p.N) continue;
+        const uint32_t off = red_base + (uint32_t)((rr * (BN + 1) + j) * 4);
+        float sum = 0.0f;
+        for (int pr = 0; pr < ks; ++pr) sum += ld_shared_cluster_f32(map_shared_rank(off, (uint32_t)pr));
+        const float bval = p.bias ? bf16_bits_to_f32(p.bias[n]) : 0.0f;
+        const float val = __fadd_rn(__fmul_rn(sum, gsc), bval);
+        const int64_t m = m0 + j;
+        if (p.out_f32)
+          reinterpret_cast<float*>(p.y)[m * p.N + n] = val;
+        else
+          reinterpret_cast<__nv_bfloat16*>(p.y)[m * p.N + n] = __float2bfloat16_rn(val);
+      }
+    }
+    __syncwarp();
+    cluster_sync();
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, T::ALLOC);
+  }
+}
+
+template <int BN, int STAGES, int FMT>
+int launch_tc(const LinearArgs& a, cudaStream_t s, int ksplit) {
+  using S = Smem<BN, STAGES, FMT>;
+  auto kern = wq_tc_kernel<BN, STAGES, FMT>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
+  if (attr_err != cudaSuccess) return WQ_ERR_CUDA;
+
+  alignas(64) CUtensorMap tmX, tmW;
+  const uint64_t wrow = (uint64_t)(FMT == WQ_Q8_0 ? a.K : a.K / 2);
+  if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M,
+                      (uint64_t)a.K * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return WQ_ERR_CUDA;
+  if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, wrow, (uint64_t)a.N, wrow,
+                      Fmt<FMT>::WB, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return WQ_ERR_CUDA;
+
+  TcParams p;
+  p.scales = a.scales;
+  p.bias = a.bias;
+  p.y = a.y;
+  p.M = (int)a.M;
+  p.N = (int)a.N;
+  p.K = (int)a.K;
+  p.out_f32 = a.out_f32 ? 1 : 0;
+  p.ksplit = ksplit;
+  p.weights_static = a.weights_static ? 1 : 0;
+  p.lay = scales_layout(FMT, a.N, a.K);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((a.N + kRows - 1) / kRows), (unsigned)((a.M + BN - 1) / BN), (unsigned)ksplit);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = S::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  if (ksplit > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = (unsigned)ksplit;
+    ++na;
+  }
+  if (a.weights_static) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmX, tmW, p);
+  count_launch();
+  return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+constexpr int kDecodeStages = 12;
+constexpr int kGemmStages = 4;
+
+template <int FMT>
+int dispatch_fmt(const LinearArgs& a, cudaStream_t s) {
+  const int nchunks = (int)(a.K / kKS);
+  const int ntiles = (int)((a.N + kRows - 1) / kRows);
+  if (a.M <= 16) {
+    // split K over a cluster so that the grid covers the GPU (152 SMs)
+    int ks = (2 * 152 + ntiles - 1) / ntiles;
+    if (ks > 8) ks = 8;
+    if (ks > nchunks) ks = nchunks;
+    if (ks < 1) ks = 1;
+    return launch_tc<16, kDecodeStages, FMT>(a, s, ks);
+  }
+  if (a.M <= 64) return launch_tc<64, kGemmStages, FMT>(a, s, 1);
+  const int64_t tiles256 = ((a.M + 255) / 256) * ntiles;
+  if (tiles256 < 152) return launch_tc<128, kGemmStages, FMT>(a, s, 1);
+  return launch_tc<256, kGemmStages, FMT>(a, s, 1);
+}
+
+}  // namespace
+
+int linear_tc(const LinearArgs& a, cudaStream_t s, int* rc) {
+  // size rules of this path; anything else falls back to the CUDA-core kernel
+  if (a.K % kKS != 0 || a.K < kKS) return 0;
+  if (a.M > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF) return 0;
+  if (((uintptr_t)a.x & 15u) != 0) return 0;
+  switch (a.fmt) {
+    case WQ_NF4: *rc = dispatch_fmt<WQ_NF4>(a, s); return 1;
+    case WQ_NVFP4: *rc = dispatch_fmt<WQ_NVFP4>(a, s); return 1;
+    case WQ_Q4_0: *rc = dispatch_fmt<WQ_Q4_0>(a, s); return 1;
+    case WQ_Q8_0: *rc = dispatch_fmt<WQ_Q8_0>(a, s); return 1;
+    default: return 0;
+  }
+}
+
+int take_status_tc() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return WQ_ERR_CUDA;
+  cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace wq

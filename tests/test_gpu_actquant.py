@@ -1,0 +1,34 @@
+"""NVFP4 runtime activation quantiser against the oracle: bit-exact codes, scales and g."""
+import numpy as np
+import pytest
+import torch
+
+from bit_weight_quantized_matmul_gb300 import workloads as wl
+from oracle import quant as Q
+from tests.gpu_common import wq, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("M,K,seed", [(1, 1280, 100), (37, 384, 1), (1500, 1280, 100), (1500, 5120, 102),
+                                      (6000, 1280, 101), (3, 32, 7)])
+@pytest.mark.parametrize("static_g", [False, True])
+def test_act_quant_bit_exact(M, K, seed, static_g):
+    need_gpu()
+    x = wl.activations(seed, M, K, outlier_frac=0.001)
+    xf = wl.bf16_as_f32(x)
+    g_in = np.float32(0.0031) if static_g else None
+    ref = Q.quant_act_nvfp4(xf, g_in)
+    gt = torch.tensor([g_in], dtype=torch.float32, device="cuda") if static_g else None
+    codes, scales, g = wq().quant_act_nvfp4(x.cuda(), g_in=gt)
+    torch.cuda.synchronize()
+    assert g.item() == float(ref["g"])
+    assert np.array_equal(scales.cpu().numpy(), ref["scales"])
+    assert np.array_equal(codes.cpu().numpy().reshape(-1), Q.pack_nibbles(ref["codes"]))
+
+
+def test_act_quant_all_zero():
+    need_gpu()
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    codes, scales, g = wq().quant_act_nvfp4(x)
+    assert g.item() == 1.0 and int(codes.sum()) == 0 and int(scales.sum()) == 0

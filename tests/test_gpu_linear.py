@@ -1,0 +1,131 @@
+"""Fused dequant-matmul (tensor-core and CUDA-core paths) against the fp64 oracle.
+
+Tolerances (stated by the acceptance bar of the method): relative L2 <= 5e-3 on
+the bf16 output, max |y - y_ref| <= 1e-2 rms(y_ref) on the fp32-output mode.
+Guard rows around y catch out-of-bounds writes."""
+import numpy as np
+import pytest
+import torch
+
+from bit_weight_quantized_matmul_gb300 import workloads as wl
+from oracle import linear as L
+from oracle import quant as Q
+from tests.gpu_common import (wq, need_gpu, weight_np, oracle_pack, gpu_pack, with_guard, REL_L2_TOL,
+                              MAX_ABS_TOL)
+from tests.helpers import rel_l2, max_abs_over_rms
+
+pytestmark = pytest.mark.gpu
+
+SENT_BF16 = -12288.0  # exactly representable in bf16
+
+
+def run_case(fmt, M, N, K, seed=0, has_bias=True, outliers=0.0, force_simt=False, weights_static=False,
+             bar=True):
+    W = weight_np(seed, N, K)
+    x = wl.activations(seed, M, K, outlier_frac=outliers)
+    b = wl.bias(seed, N) if has_bias else None
+    p_ref = oracle_pack(fmt, W)
+    xf = wl.bf16_as_f32(x)
+    bf = wl.bf16_as_f32(b) if has_bias else None
+    if fmt == "nvfp4_w4a4":
+        y_ref = L.linear_w4a4(xf, p_ref, bf)
+    else:
+        y_ref = L.linear_w4a16(xf, p_ref, bf)
+    packed, scales = gpu_pack(fmt, W)
+    xg = x.cuda()
+    bg = b.cuda() if has_bias else None
+    xin = wq().quant_act_nvfp4(xg) if fmt == "nvfp4_w4a4" else xg
+    full16, y16 = with_guard((M, N), torch.bfloat16, SENT_BF16)
+    full32, y32 = with_guard((M, N), torch.float32, float("nan"))
+    wq().linear_into(y16, xin, packed, scales, fmt, N, K, bg, force_simt=force_simt, weights_static=weights_static)
+    wq().linear_into(y32, xin, packed, scales, fmt, N, K, bg, out_f32=True, force_simt=force_simt)
+    torch.cuda.synchronize()
+    assert wq().last_device_status() == 0
+    g16 = full16.float().cpu().numpy()
+    g32 = full32.cpu().numpy()
+    assert np.all(g16[0] == SENT_BF16) and np.all(g16[-1] == SENT_BF16), "write outside y (bf16)"
+    assert np.all(np.isnan(g32[0])) and np.all(np.isnan(g32[-1])), "write outside y (fp32)"
+    y16n, y32n = g16[1:-1], g32[1:-1]
+    assert np.all(np.isfinite(y32n))
+    assert rel_l2(y16n, y_ref) <= REL_L2_TOL, rel_l2(y16n, y_ref)
+    if bar:
+        assert max_abs_over_rms(y32n, y_ref) <= MAX_ABS_TOL, max_abs_over_rms(y32n, y_ref)
+    else:
+        # provable elementwise bound for a bf16-rounded weight operand (relative error <= 2^-9 per
+        # weight) with fp32 accumulation over K and two fp32 roundings in the epilogue
+        w_hat = Q.DEQUANT["nvfp4" if fmt == "nvfp4_w4a4" else fmt](p_ref).astype(np.float64)
+        mag = np.abs(xf.astype(np.float64)) @ np.abs(w_hat).T
+        bound = (2.0 ** -9 + K * 2.0 ** -23) * mag + 2.0 ** -22 * np.abs(y_ref) + 1e-6
+        assert np.all(np.abs(y32n - y_ref) <= bound), float(np.max(np.abs(y32n - y_ref) / bound))
+    # the bf16 output is the fp32 output rounded once (same kernel, final cast)
+    assert np.array_equal(torch.from_numpy(y32n).to(torch.bfloat16).float().numpy(), y16n)
+    return y32n, y_ref
+
+
+FMTS = ["nf4", "nvfp4", "q4_0", "q8_0"]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1536, 384), (1, 384, 1536),                      # whisper-tiny fc1 / fc2 (decode)
+    (1, 1280, 1280), (4, 5120, 1280), (16, 1280, 5120),  # turbo decoder shapes, M in {1, 4, 16}
+    (3, 200, 320),                                       # ragged N and K
+])
+def test_decode_path(fmt, M, N, K):
+    need_gpu()
+    run_case(fmt, M, N, K, seed=N + K + M)
+
+
+GEMM_SHAPES = [
+    (1500, 1280, 1280),                 # one 30 s window, q/k/v/o
+    (300, 5120, 1280),                  # fc1 shape, ragged M
+    (37, 1280, 5120),                   # fc2 shape, M between the decode and GEMM tiles
+    (130, 200, 256),                    # ragged everything
+]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_path(fmt, M, N, K):
+    """The acceptance bar on each format's own workload distribution: NVFP4 encoder inputs carry
+    0.1 % outliers x20; the q8_0 encoder (and NF4 / q4_0) inputs are plain N(0, 1)."""
+    need_gpu()
+    run_case(fmt, M, N, K, seed=M + N + K, outliers=0.001 if fmt == "nvfp4" else 0.0)
+
+
+@pytest.mark.parametrize("fmt", ["nf4", "q4_0", "q8_0"])
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES[:2])
+def test_gemm_path_outlier_stress(fmt, M, N, K):
+    """Outlier activations on the formats whose decoded weights are not exact in bf16: relative L2
+    still within the bar, and every element within the provable bf16-operand error bound."""
+    need_gpu()
+    run_case(fmt, M, N, K, seed=M + N + K + 1, outliers=0.001, bar=False)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_simt_path_matches_oracle(fmt):
+    need_gpu()
+    run_case(fmt, 5, 384, 1536, seed=3, force_simt=True)
+    run_case(fmt, 33, 256, 320, seed=4, force_simt=True)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1280, 1280), (16, 5120, 1280), (1500, 1280, 1280), (300, 1280, 5120)])
+def test_w4a4(M, N, K):
+    need_gpu()
+    run_case("nvfp4_w4a4", M, N, K, seed=100 + M, outliers=0.001)
+
+
+def test_no_bias_and_static_weights_flag():
+    need_gpu()
+    run_case("nf4", 16, 1280, 1280, seed=9, has_bias=False, weights_static=True)
+    run_case("q4_0", 1, 5120, 1280, seed=10, has_bias=True, weights_static=True)
+
+
+def test_m_zero_is_noop():
+    need_gpu()
+    W = weight_np(0, 128, 128)
+    packed, scales = gpu_pack("nf4", W)
+    x = torch.zeros((0, 128), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((0, 128), dtype=torch.bfloat16, device="cuda")
+    wq().linear_into(y, x, packed, scales, "nf4", 128, 128)
+    torch.cuda.synchronize()
