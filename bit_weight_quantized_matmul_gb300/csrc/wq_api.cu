@@ -34,7 +34,7 @@ ScalesLayout scales_layout(int fmt, int64_t N, int64_t K) {
       break;
     case WQ_Q4_0:
     case WQ_Q8_0:
-      L.total = (size_t)(n / 32) * 2;
+      L.total = align16((size_t)(n / 32) * 2);
       break;
     default:
       break;
@@ -195,10 +195,60 @@ int wq_linear_ex(const void* x, const void* packed, const void* scales, int fmt,
   a.weights_static = (flags & WQ_FLAG_WEIGHTS_STATIC) != 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!(flags & WQ_FLAG_FORCE_SIMT)) {
-    int handled = fmt == WQ_NVFP4_W4A4 ? linear_w4a4_tc(a, s, &rc) : linear_tc(a, s, &rc);
-    if (handled) return rc;
+    if (fmt == WQ_NVFP4_W4A4) {
+      if (linear_w4a4_tc(a, s, &rc)) return rc;
+    } else if (M <= 16) {
+      if (linear_tc(a, s, &rc)) return rc;
+    } else if (tcp_eligible(a)) {
+      return linear_tcp(&a, 1, s);
+    }
   }
   return linear_simt(a, s);
+}
+
+int wq_linear_grouped(const wq_problem* problems, int count, int fmt, unsigned flags, void* stream) {
+  if (!problems || count < 1 || count > WQ_GROUP_MAX) return WQ_ERR_ARG;
+  if (flags & ~(unsigned)(WQ_FLAG_OUT_F32 | WQ_FLAG_WEIGHTS_STATIC)) return WQ_ERR_ARG;
+  if (fmt == WQ_NVFP4_W4A4) return WQ_ERR_FMT;
+  LinearArgs args[WQ_GROUP_MAX];
+  int n = 0;
+  bool all_tc = true;
+  for (int i = 0; i < count; ++i) {
+    const wq_problem& p = problems[i];
+    int rc = check_weight(fmt, p.N, p.K);
+    if (rc != WQ_OK) return rc;
+    if (p.M < 0) return WQ_ERR_ARG;
+    if (p.M == 0 || p.N == 0) continue;
+    if (!p.x || !p.packed || !p.scales || !p.y) return WQ_ERR_ARG;
+    if (!aligned16(p.x) || !aligned16(p.packed) || !aligned16(p.scales) || !aligned16(p.y) ||
+        (p.bias && !aligned16(p.bias)))
+      return WQ_ERR_ALIGN;
+    LinearArgs a{};
+    a.x = p.x;
+    a.packed = reinterpret_cast<const uint8_t*>(p.packed);
+    a.scales = reinterpret_cast<const uint8_t*>(p.scales);
+    a.fmt = fmt;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.bias = p.bias;
+    a.y = p.y;
+    a.out_f32 = (flags & WQ_FLAG_OUT_F32) != 0;
+    a.weights_static = (flags & WQ_FLAG_WEIGHTS_STATIC) != 0;
+    all_tc = all_tc && tcp_eligible(a);
+    args[n++] = a;
+  }
+  if (n == 0) return WQ_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (all_tc) return linear_tcp(args, n, s);
+  for (int i = 0; i < n; ++i) {  // some problem outside the tensor-core rules: one call each
+    const wq_problem& p = problems[i];
+    int rc = wq_linear_ex(args[i].x, args[i].packed, args[i].scales, fmt, args[i].M, args[i].N, args[i].K,
+                          args[i].bias, args[i].y, flags, stream);
+    (void)p;
+    if (rc != WQ_OK) return rc;
+  }
+  return WQ_OK;
 }
 
 int wq_linear(const void* x, const void* packed, const void* scales, int fmt, int64_t M, int64_t N, int64_t K,
@@ -209,7 +259,8 @@ int wq_linear(const void* x, const void* packed, const void* scales, int fmt, in
 int wq_last_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
   int worst = WQ_OK;
-  const int parts[4] = {take_status_pack(), take_status_simt(), take_status_tc(), take_status_w4a4()};
+  const int parts[5] = {take_status_pack(), take_status_simt(), take_status_tc(), take_status_tcp(),
+                        take_status_w4a4()};
   for (int v : parts)
     if (v != WQ_OK) worst = v;
   return worst;

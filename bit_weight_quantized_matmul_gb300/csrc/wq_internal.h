@@ -55,7 +55,12 @@ struct LinearArgs {
 int linear_simt(const LinearArgs& a, cudaStream_t s);
 int take_status_simt();
 
-// ---- linear: tensor-core paths (wq_tc.cu, wq_w4a4.cu)
+// ---- linear: tensor-core paths (wq_tc.cu: decode split-K; wq_tcp.cu: persistent work list;
+//      wq_w4a4.cu: block-scaled FP4)
+constexpr int kGroupMax = WQ_GROUP_MAX;
+bool tcp_eligible(const LinearArgs& a);
+int linear_tcp(const LinearArgs* probs, int count, cudaStream_t s);
+int take_status_tcp();
 // return 1 = handled (status in *rc), 0 = shape not eligible for this path
 int linear_tc(const LinearArgs& a, cudaStream_t s, int* rc);
 int take_status_tc();

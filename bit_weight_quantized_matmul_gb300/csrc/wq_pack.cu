@@ -244,9 +244,15 @@ __global__ void nvfp4_finalize_kernel(float* slot, uint8_t* pad_begin, int pad_l
 }
 
 // ------------------------------------------------------------------ q4_0 / q8_0
+// zero the bytes between the last fp16 d and the 16-byte aligned end of the scales blob
+__device__ __forceinline__ void zero_d_pad(uint16_t* d_out, int64_t nb) {
+  for (int64_t i = nb; i % 8 != 0; ++i) d_out[i] = 0;
+}
+
 __global__ void q4_0_kernel(const float* __restrict__ W, int64_t nb, uint8_t* __restrict__ packed,
                             uint16_t* __restrict__ d_out) {
   const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0) zero_d_pad(d_out, nb);
   if (b >= nb) return;
   const float4* src = reinterpret_cast<const float4*>(W + b * kGGBlock);
   float v[kGGBlock];
@@ -275,6 +281,7 @@ __global__ void q4_0_kernel(const float* __restrict__ W, int64_t nb, uint8_t* __
 __global__ void q8_0_kernel(const float* __restrict__ W, int64_t nb, int8_t* __restrict__ packed,
                             uint16_t* __restrict__ d_out) {
   const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0) zero_d_pad(d_out, nb);
   if (b >= nb) return;
   const float4* src = reinterpret_cast<const float4*>(W + b * kGGBlock);
   float v[kGGBlock];

@@ -26,12 +26,12 @@
 
 #include "wq_device.cuh"
 #include "wq_internal.h"
+#include "wq_tc_common.cuh"
 
 namespace wq {
 namespace {
 
-constexpr int kKS = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16 x)
-constexpr int kRows = 128;     // weight rows per tile (the MMA M)
+using namespace tc;
 constexpr int kNA = 4;         // TMEM A-operand ring slots (32 columns each)
 constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 dequant + epilogue
 
@@ -44,11 +44,6 @@ struct TcParams {
   int ksplit;            // CTAs along K (a cluster when > 1)
   int weights_static;    // programmatic dependent launch: stream W before the dependency resolves
   ScalesLayout lay;
-};
-
-template <int FMT>
-struct Fmt {
-  static constexpr int WB = (FMT == WQ_Q8_0) ? 64 : 32;  // packed bytes per row per stage
 };
 
 template <int BN, int STAGES, int FMT>
@@ -72,90 +67,6 @@ struct TmemCols {
   static constexpr int USED = D_COL + BN;
   static constexpr int ALLOC = USED <= 256 ? 256 : 512;
 };
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-// Byte -> (value of low nibble, value of high nibble) for the 4-bit formats.
-template <int FMT>
-__device__ __forceinline__ float nibble_value(uint32_t c) {
-  if (FMT == WQ_NF4) return kNF4[c];
-  if (FMT == WQ_Q4_0) return (float)((int)c - 8);
-  return kE2M1[c];  // NVFP4: E2M1 value; the E4M3 block scale multiplies it, g is applied on D
-}
-
-// Decode the 64 weights [k0, k0 + 64) of row n into 32 bf16x2 words.
-template <int FMT>
-__device__ __forceinline__ void decode_chunk(const TcParams& p, const uint8_t* wrow, const float2* lut, int64_t n,
-                                             int64_t k0, bool row_ok, uint32_t (&out)[32]) {
-  if (FMT == WQ_Q8_0) {
-    float d0 = 0.0f, d1 = 0.0f;
-    if (row_ok) {
-      const uint32_t dd = *reinterpret_cast<const uint32_t*>(p.scales + 2 * ((n * p.K + k0) / 32));
-      d0 = f16_bits_to_f32(dd & 0xFFFFu);
-      d1 = f16_bits_to_f32(dd >> 16);
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(wrow);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = src[q];
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-      const float d = (q < 2) ? d0 : d1;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a0 = (float)(int8_t)(u[j] & 0xFF), a1 = (float)(int8_t)((u[j] >> 8) & 0xFF);
-        const float a2 = (float)(int8_t)((u[j] >> 16) & 0xFF), a3 = (float)(int8_t)(u[j] >> 24);
-        out[q * 8 + j * 2] = pack_bf16x2(__fmul_rn(a0, d), __fmul_rn(a1, d));
-        out[q * 8 + j * 2 + 1] = pack_bf16x2(__fmul_rn(a2, d), __fmul_rn(a3, d));
-      }
-    }
-    return;
-  }
-  // 4-bit formats: 32 bytes, element 2j in the low nibble of byte j
-  float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // scale per 16 elements of the chunk
-  if (row_ok) {
-    if (FMT == WQ_NF4) {
-      const int64_t b = (n * p.K + k0) / 64;
-      const int8_t q = reinterpret_cast<const int8_t*>(p.scales)[b];
-      const float s2 = reinterpret_cast<const float*>(p.scales + p.lay.s2_off)[b / 256];
-      const float off = *reinterpret_cast<const float*>(p.scales + p.lay.offset_off);
-      const float a = __fadd_rn(__fmul_rn((float)q, s2), off);
-      sc[0] = sc[1] = sc[2] = sc[3] = a;
-    } else if (FMT == WQ_Q4_0) {
-      const uint32_t dd = *reinterpret_cast<const uint32_t*>(p.scales + 2 * ((n * p.K + k0) / 32));
-      sc[0] = sc[1] = f16_bits_to_f32(dd & 0xFFFFu);
-      sc[2] = sc[3] = f16_bits_to_f32(dd >> 16);
-    } else {  // NVFP4
-      const uint32_t s4 = *reinterpret_cast<const uint32_t*>(p.scales + (n * p.K + k0) / 16);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sc[j] = e4m3_to_f32((s4 >> (8 * j)) & 0xFFu);
-    }
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(wrow);
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint4 v = src[q];
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int byte_idx = q * 16 + j * 4 + b;  // elements 2*byte_idx, 2*byte_idx + 1
-        const float2 lv = lut[(u[j] >> (8 * b)) & 0xFFu];
-        const float s = sc[byte_idx >> 3];
-        out[byte_idx] = pack_bf16x2(__fmul_rn(lv.x, s), __fmul_rn(lv.y, s));
-      }
-    }
-  }
-}
 
 template <int BN, int STAGES, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -257,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&full[s], (i / STAGES) & 1, abort_flag)) break;
       if (i >= kNA && !mbar_wait(&aempty[slot], ((i / kNA) & 1) ^ 1, abort_flag)) break;
       uint32_t v[32];
-      decode_chunk<FMT>(p, smem + S::W_OFF + s * S::WB + r * Fmt<FMT>::WB, lut, n,
+      decode_chunk<FMT>(p.scales, p.K, p.lay, smem + S::W_OFF + s * S::WB + r * Fmt<FMT>::WB, lut, n,
                         (int64_t)(kc_begin + i) * kKS, row_ok, v);
       tmem_st32(tmem_base + lane_base + slot * 32, v);
       tc_wait_st();
@@ -405,30 +316,24 @@ int launch_tc(const LinearArgs& a, cudaStream_t s, int ksplit) {
 }
 
 constexpr int kDecodeStages = 12;
-constexpr int kGemmStages = 4;
 
 template <int FMT>
 int dispatch_fmt(const LinearArgs& a, cudaStream_t s) {
   const int nchunks = (int)(a.K / kKS);
   const int ntiles = (int)((a.N + kRows - 1) / kRows);
-  if (a.M <= 16) {
-    // split K over a cluster so that the grid covers the GPU (152 SMs)
-    int ks = (2 * 152 + ntiles - 1) / ntiles;
-    if (ks > 8) ks = 8;
-    if (ks > nchunks) ks = nchunks;
-    if (ks < 1) ks = 1;
-    return launch_tc<16, kDecodeStages, FMT>(a, s, ks);
-  }
-  if (a.M <= 64) return launch_tc<64, kGemmStages, FMT>(a, s, 1);
-  const int64_t tiles256 = ((a.M + 255) / 256) * ntiles;
-  if (tiles256 < 152) return launch_tc<128, kGemmStages, FMT>(a, s, 1);
-  return launch_tc<256, kGemmStages, FMT>(a, s, 1);
+  // split K over a cluster so that the grid covers the GPU (152 SMs)
+  int ks = (2 * 152 + ntiles - 1) / ntiles;
+  if (ks > 8) ks = 8;
+  if (ks > nchunks) ks = nchunks;
+  if (ks < 1) ks = 1;
+  return launch_tc<16, kDecodeStages, FMT>(a, s, ks);
 }
 
 }  // namespace
 
 int linear_tc(const LinearArgs& a, cudaStream_t s, int* rc) {
-  // size rules of this path; anything else falls back to the CUDA-core kernel
+  // decode-sized M only; size rules of this path, anything else falls back to the CUDA-core kernel
+  if (a.M > 16) return 0;
   if (a.K % kKS != 0 || a.K < kKS) return 0;
   if (a.M > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF) return 0;
   if (((uintptr_t)a.x & 15u) != 0) return 0;

@@ -1,0 +1,225 @@
+// wq_tc_common.cuh -- device pieces shared by the tensor-core kernels: per-format
+// weight decoding into bf16 pairs for the MMA A operand held in tensor memory.
+#pragma once
+#include "wq_device.cuh"
+#include "wq_internal.h"
+
+namespace wq {
+namespace tc {
+
+constexpr int kKS = 64;    // K per pipeline chunk (one 128-byte swizzle row of bf16 x)
+constexpr int kRows = 128; // weight rows per tile (the MMA M)
+
+template <int FMT>
+struct Fmt {
+  static constexpr int WB = (FMT == WQ_Q8_0) ? 64 : 32;  // packed bytes per row per stage
+};
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// Byte -> (value of low nibble, value of high nibble) for the 4-bit formats.
+template <int FMT>
+__device__ __forceinline__ float nibble_value(uint32_t c) {
+  if (FMT == WQ_NF4) return kNF4[c];
+  if (FMT == WQ_Q4_0) return (float)((int)c - 8);
+  return kE2M1[c];  // NVFP4: E2M1 value; the E4M3 block scale multiplies it, g is applied on D
+}
+
+// Decode the 64 weights [k0, k0 + 64) of row n into 32 bf16x2 words.
+template <int FMT>
+__device__ __forceinline__ void decode_chunk(const uint8_t* __restrict__ scales, int64_t K, const ScalesLayout& lay,
+                                             const uint8_t* wrow, const float2* lut, int64_t n, int64_t k0,
+                                             bool row_ok, uint32_t (&out)[32]) {
+  if (FMT == WQ_Q8_0) {
+    float d0 = 0.0f, d1 = 0.0f;
+    if (row_ok) {
+      const uint32_t dd = *reinterpret_cast<const uint32_t*>(scales + 2 * ((n * K + k0) / 32));
+      d0 = f16_bits_to_f32(dd & 0xFFFFu);
+      d1 = f16_bits_to_f32(dd >> 16);
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(wrow);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = src[q];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      const float d = (q < 2) ? d0 : d1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a0 = (float)(int8_t)(u[j] & 0xFF), a1 = (float)(int8_t)((u[j] >> 8) & 0xFF);
+        const float a2 = (float)(int8_t)((u[j] >> 16) & 0xFF), a3 = (float)(int8_t)(u[j] >> 24);
+        out[q * 8 + j * 2] = pack_bf16x2(__fmul_rn(a0, d), __fmul_rn(a1, d));
+        out[q * 8 + j * 2 + 1] = pack_bf16x2(__fmul_rn(a2, d), __fmul_rn(a3, d));
+      }
+    }
+    return;
+  }
+  // 4-bit formats: 32 bytes, element 2j in the low nibble of byte j
+  float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // scale per 16 elements of the chunk
+  if (row_ok) {
+    if (FMT == WQ_NF4) {
+      const int64_t b = (n * K + k0) / 64;
+      const int8_t q = reinterpret_cast<const int8_t*>(scales)[b];
+      const float s2 = reinterpret_cast<const float*>(scales + lay.s2_off)[b / 256];
+      const float off = *reinterpret_cast<const float*>(scales + lay.offset_off);
+      const float a = __fadd_rn(__fmul_rn((float)q, s2), off);
+      sc[0] = sc[1] = sc[2] = sc[3] = a;
+    } else if (FMT == WQ_Q4_0) {
+      const uint32_t dd = *reinterpret_cast<const uint32_t*>(scales + 2 * ((n * K + k0) / 32));
+      sc[0] = sc[1] = f16_bits_to_f32(dd & 0xFFFFu);
+      sc[2] = sc[3] = f16_bits_to_f32(dd >> 16);
+    } else {  // NVFP4
+      const uint32_t s4 = *reinterpret_cast<const uint32_t*>(scales + (n * K + k0) / 16);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[j] = e4m3_to_f32((s4 >> (8 * j)) & 0xFFu);
+    }
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(wrow);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint4 v = src[q];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int byte_idx = q * 16 + j * 4 + b;  // elements 2*byte_idx, 2*byte_idx + 1
+        const float2 lv = lut[(u[j] >> (8 * b)) & 0xFFu];
+        const float s = sc[byte_idx >> 3];
+        out[byte_idx] = pack_bf16x2(__fmul_rn(lv.x, s), __fmul_rn(lv.y, s));
+      }
+    }
+  }
+}
+
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// The per-(row, 64-chunk) scale word staged in shared memory for the dequant warps:
+//   NF4         the decoded block absmax a_hat = q * s2 + offset (fp32 bits; one 64-block per chunk)
+//   NVFP4       the four E4M3 block-scale bytes of the chunk (one per 16 elements)
+//   q4_0, q8_0  the two fp16 d of the chunk (one per 32 elements)
+// For the last three the word is the 4 bytes at offset n*K/16 + 4c of the scales blob.
+template <int FMT>
+__device__ __forceinline__ uint32_t scale_word(const uint8_t* __restrict__ scales, const ScalesLayout& lay,
+                                               int64_t K, int64_t n, int64_t c) {
+  if (FMT == WQ_NF4) {
+    const int64_t b = n * (K / 64) + c;
+    const int8_t q = reinterpret_cast<const int8_t*>(scales)[b];
+    const float s2 = reinterpret_cast<const float*>(scales + lay.s2_off)[b / 256];
+    const float off = *reinterpret_cast<const float*>(scales + lay.offset_off);
+    return __float_as_uint(__fadd_rn(__fmul_rn((float)q, s2), off));
+  }
+  return *reinterpret_cast<const uint32_t*>(scales + n * (K / 16) + 4 * c);
+}
+
+// Decode half h (elements [32h, 32h + 32)) of one 64-element chunk of a weight row
+// into 16 bf16x2 words.  `wrow` points at the row's packed chunk in shared memory.
+template <int FMT>
+__device__ __forceinline__ void decode_half(uint32_t sword, const uint8_t* wrow, const float2* lut, int h,
+                                            uint32_t (&out)[16]) {
+  if (FMT == WQ_Q8_0) {
+    const float d = f16_bits_to_f32(h ? (sword >> 16) : (sword & 0xFFFFu));
+    const uint4* src = reinterpret_cast<const uint4*>(wrow + 32 * h);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 v = src[q];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a0 = (float)(int8_t)(u[j] & 0xFF), a1 = (float)(int8_t)((u[j] >> 8) & 0xFF);
+        const float a2 = (float)(int8_t)((u[j] >> 16) & 0xFF), a3 = (float)(int8_t)(u[j] >> 24);
+        out[q * 8 + j * 2] = pack_bf16x2(__fmul_rn(a0, d), __fmul_rn(a1, d));
+        out[q * 8 + j * 2 + 1] = pack_bf16x2(__fmul_rn(a2, d), __fmul_rn(a3, d));
+      }
+    }
+    return;
+  }
+  float sc0, sc1;  // scale of elements [0, 16) and [16, 32) of this half
+  if (FMT == WQ_NF4) {
+    sc0 = sc1 = __uint_as_float(sword);
+  } else if (FMT == WQ_Q4_0) {
+    sc0 = sc1 = f16_bits_to_f32(h ? (sword >> 16) : (sword & 0xFFFFu));
+  } else {
+    sc0 = e4m3_to_f32((sword >> (16 * h)) & 0xFFu);
+    sc1 = e4m3_to_f32((sword >> (16 * h + 8)) & 0xFFu);
+  }
+  const uint4 v = *reinterpret_cast<const uint4*>(wrow + 16 * h);
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float s = (j < 2) ? sc0 : sc1;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 lv = lut[(u[j] >> (8 * b)) & 0xFFu];
+      out[j * 4 + b] = pack_bf16x2(__fmul_rn(lv.x, s), __fmul_rn(lv.y, s));
+    }
+  }
+}
+
+// Decode NE (32 or 64) consecutive weights of one 64-element block of a row into NE/2
+// bf16x2 words.  `part` selects which NE-element part of the block (0 when NE == 64);
+// `sword` is the block's scale word (see scale_word); `wsrc` points at the NE packed
+// codes in shared memory.  The byte -> (value, value) table holds LUTREP copies
+// interleaved so that lane group `lsel` reads its own banks (LUTREP = 16: the 16
+// lanes of a half-warp never collide on a 64-bit load, whatever the codes).
+template <int FMT, int NE, int LUTREP>
+__device__ __forceinline__ void decode_span(uint32_t sword, int part, const uint8_t* wsrc, const float2* lut,
+                                            int lsel, uint32_t (&out)[NE / 2]) {
+  static_assert(NE == 32 || NE == 64, "span");
+  if (FMT == WQ_Q8_0) {
+#pragma unroll
+    for (int q = 0; q < NE / 16; ++q) {
+      const int e0 = part * NE + q * 16;  // element index within the 64-block
+      const float d = f16_bits_to_f32(e0 < 32 ? (sword & 0xFFFFu) : (sword >> 16));
+      const uint4 v = reinterpret_cast<const uint4*>(wsrc)[q];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a0 = (float)(int8_t)(u[j] & 0xFF), a1 = (float)(int8_t)((u[j] >> 8) & 0xFF);
+        const float a2 = (float)(int8_t)((u[j] >> 16) & 0xFF), a3 = (float)(int8_t)(u[j] >> 24);
+        out[q * 8 + j * 2] = pack_bf16x2(__fmul_rn(a0, d), __fmul_rn(a1, d));
+        out[q * 8 + j * 2 + 1] = pack_bf16x2(__fmul_rn(a2, d), __fmul_rn(a3, d));
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int q = 0; q < NE / 32; ++q) {
+    const uint4 v = reinterpret_cast<const uint4*>(wsrc)[q];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e0 = part * NE + q * 32 + j * 8;  // first element of this word within the 64-block
+      float s;
+      if (FMT == WQ_NF4) s = __uint_as_float(sword);
+      else if (FMT == WQ_Q4_0) s = f16_bits_to_f32(e0 < 32 ? (sword & 0xFFFFu) : (sword >> 16));
+      else s = e4m3_to_f32((sword >> (8 * (e0 / 16))) & 0xFFu);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float2 lv = lut[((u[j] >> (8 * b)) & 0xFFu) * LUTREP + lsel];
+        out[q * 16 + j * 4 + b] = pack_bf16x2(__fmul_rn(lv.x, s), __fmul_rn(lv.y, s));
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&v)[16]) { tmem_st16(taddr, v); }
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&v)[32]) { tmem_st32(taddr, v); }
+
+}  // namespace tc
+}  // namespace wq

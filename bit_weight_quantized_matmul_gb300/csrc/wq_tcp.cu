@@ -1,0 +1,506 @@
+// wq_tcp.cu -- persistent tensor-core fused dequantise-and-multiply over a work
+// list of (Linear, 128-row weight tile, BN-row activation tile) items.
+//
+// Serves two calls:
+//   * wq_linear for M > 16 (encoder-sized activations, e.g. 1500 frames per
+//     30 s window): one problem, items = n-tiles x m-tiles;
+//   * wq_linear_grouped: many independent Linears of one format in ONE launch
+//     (the fused Q/K/V projection of PR "Run quantized Whisper on the fused
+//     Metal decode path", "Summary", generalised to any set of Linears whose
+//     inputs are ready), so that the weight stream of every Linear in the group
+//     shares one pipeline instead of paying a kernel boundary each.
+//
+// Per CTA (one per SM, persistent), warp-specialised:
+//   warp 0      TMA producer: packed weight tile [128 x 64 codes] and x tile
+//               [BN x 64] (128-byte swizzle) per K chunk, STAGES-deep ring.
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma.kind::f16, A = decoded
+//               weights in TMEM, B = x in shared memory, D in TMEM, double
+//               buffered across items so the epilogue of one item overlaps the
+//               main loop of the next.
+//   warps 2..9  dequant: two warps per TMEM lane quarter, one thread per weight
+//               row and half chunk, packed codes -> bf16 pairs -> tcgen05.st
+//               into a 4-slot TMEM ring.
+//   warps 10..13 epilogue: tcgen05.ld, x global scale (NVFP4), + bias, store y.
+//   warp 14     scale stager: one item ahead, copies the tile's per-(row, chunk)
+//               scale words into shared memory chunk-major (conflict-free reads;
+//               NF4's second-level decode q * s2 + offset is done here).
+// Every item covers the whole K range, so no cross-CTA reduction is needed.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "wq_device.cuh"
+#include "wq_internal.h"
+#include "wq_tc_common.cuh"
+
+namespace wq {
+namespace {
+
+using namespace tc;
+
+constexpr int kNA = 4;            // TMEM A ring slots
+constexpr int kDeqWarps = 8;      // two per TMEM lane quarter, each decoding half of a chunk
+constexpr int kEpiWarp0 = 2 + kDeqWarps;
+constexpr int kScaleWarp = kEpiWarp0 + 4;
+constexpr int kPThreads = (kScaleWarp + 1) * 32;  // 15 warps
+constexpr int kMaxChunks = 80;    // 64-element blocks per row: K <= 5120 on this path
+constexpr int kS2Max = 48;        // NF4: s2 values a tile can touch (128 * 80 / 256 + 2) + offset
+
+struct PProblem {
+  const uint8_t* scales;
+  const uint16_t* bias;
+  void* y;
+  int M, N, K;
+  int ntiles, mtiles;
+  int item_begin;
+  ScalesLayout lay;
+};
+
+struct PParams {
+  int nprob, total_items, out_f32, weights_static;
+  int sc_bytes;  // bytes per scale buffer (max over the problems)
+  PProblem prob[kGroupMax];
+};
+
+struct PMaps {
+  CUtensorMap w[kGroupMax];
+  CUtensorMap x[kGroupMax];
+};
+
+// KC: K elements per pipeline chunk (64 or 128: one or two 128-byte swizzle rows of x)
+template <int BN, int STAGES, int FMT, int KC, int LUTREP>
+struct PSmem {
+  static constexpr int SUB = KC / 64;
+  static constexpr int XB = SUB * BN * 128;
+  static constexpr int WB = kRows * Fmt<FMT>::WB * SUB;
+  static constexpr int X_OFF = 0;
+  static constexpr int W_OFF = X_OFF + STAGES * XB;
+  static constexpr int LUT_OFF = W_OFF + STAGES * WB;
+  static constexpr int LUT_BYTES = (FMT == WQ_Q8_0) ? 0 : 256 * 8 * LUTREP;
+  static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
+  static constexpr int NBAR = 2 * STAGES + 2 * kNA + 8;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int S2_OFF = (MISC_OFF + 16 + 15) / 16 * 16;               // [2][kS2Max] NF4 s2 + offset
+  static constexpr int SC_OFF = (S2_OFF + 2 * kS2Max * 4 + 127) / 128 * 128;  // [2] raw scale slices
+  static constexpr int FIXED = SC_OFF + 1024;                                   // + alignment slack
+  // one tile's scale bytes as stored in the blob (row-major): 4 bytes per row per
+  // 64-block (NVFP4 / q4_0 / q8_0), 1 byte (NF4); two buffers
+  static constexpr int sc_bytes(int blocks) { return blocks * kRows * (FMT == WQ_NF4 ? 1 : 4); }
+  static constexpr int total(int blocks) { return FIXED + 2 * sc_bytes(blocks); }
+  static_assert(total(kMaxChunks) <= 227 * 1024, "shared memory budget");
+};
+
+template <int BN, int KC>
+struct PTmem {
+  static constexpr int ACOLS = KC / 2;  // 32-bit columns per A slot (bf16 pairs)
+  static constexpr int D_COL = kNA * ACOLS;
+  static constexpr int USED = D_COL + 2 * BN;
+  static constexpr int ALLOC = USED <= 256 ? 256 : 512;
+  static_assert(USED <= 512, "TMEM budget");
+};
+
+struct ItemCoord {
+  int p, nt, mt;
+};
+
+__device__ __forceinline__ ItemCoord item_coord(const PParams& P, int i) {
+  int p = 0;
+  while (p + 1 < P.nprob && P.prob[p + 1].item_begin <= i) ++p;
+  const int local = i - P.prob[p].item_begin;
+  const int nt_count = P.prob[p].ntiles;
+  return ItemCoord{p, local % nt_count, local / nt_count};
+}
+
+template <int BN, int STAGES, int FMT, int KC, int LUTREP>
+__global__ void __launch_bounds__(kPThreads, 1)
+    wq_tcp_kernel(const __grid_constant__ PMaps maps, const __grid_constant__ PParams P) {
+  using S = PSmem<BN, STAGES, FMT, KC, LUTREP>;
+  using T = PTmem<BN, KC>;
+  constexpr int SUB = S::SUB;
+  constexpr int NE = KC / 2;  // elements of a row each dequant warp decodes per chunk
+  constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
+  constexpr uint32_t STAGE_TX = (uint32_t)(S::XB + S::WB);
+  constexpr int WCHUNK = Fmt<FMT>::WB * SUB;  // packed bytes of one row per chunk
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* afull = bars + 2 * STAGES;
+  uint64_t* aempty = afull + kNA;
+  uint64_t* dfull = aempty + kNA;  // [2]
+  uint64_t* dempty = dfull + 2;    // [2]
+  uint64_t* sfull = dempty + 2;    // [2]
+  uint64_t* sempty = sfull + 2;    // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
+  float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
+  uint8_t* scbuf = smem + S::SC_OFF;
+  float* s2buf = reinterpret_cast<float*>(smem + S::S2_OFF);
+
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1 + kDeqWarps); }
+    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&dfull[i], 1);
+      mbar_init(&dempty[i], 4);
+      mbar_init(&sfull[i], 32);
+      mbar_init(&sempty[i], kDeqWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (FMT != WQ_Q8_0) {
+    for (int i = threadIdx.x; i < 256 * LUTREP; i += kPThreads) {
+      const uint32_t b = (uint32_t)(i / LUTREP);
+      lut[i] = make_float2(nibble_value<FMT>(b & 15u), nibble_value<FMT>(b >> 4));
+    }
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, T::ALLOC);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  griddep_launch_dependents();
+
+  const int total = P.total_items;
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int i = 0; i < P.nprob; ++i) {
+        prefetch_tmap(&maps.w[i]);
+        prefetch_tmap(&maps.x[i]);
+      }
+      // weights of the first STAGES chunks may stream before the preceding kernel finishes
+      int pre = 0;
+      if (P.weights_static) {
+        int g = 0;
+        for (int it = blockIdx.x; it < total && g < STAGES; it += gridDim.x) {
+          const ItemCoord ic = item_coord(P, it);
+          const int nch = (P.prob[ic.p].K + KC - 1) / KC;
+          for (int c = 0; c < nch && g < STAGES; ++c, ++g) {
+            mbar_arrive_expect_tx(&full[g], STAGE_TX);
+            tma_load_2d(smem + S::W_OFF + g * S::WB, &maps.w[ic.p], &full[g], c * WCHUNK, ic.nt * kRows);
+          }
+        }
+        pre = g;
+      }
+      griddep_wait();
+      int g = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const ItemCoord ic = item_coord(P, it);
+        const int nch = (P.prob[ic.p].K + KC - 1) / KC;
+        for (int c = 0; c < nch; ++c, ++g) {
+          const int s = g % STAGES;
+          if (g >= pre) {
+            if (g >= STAGES && !mbar_wait(&empty[s], ((g / STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(&full[s], STAGE_TX);
+            tma_load_2d(smem + S::W_OFF + s * S::WB, &maps.w[ic.p], &full[s], c * WCHUNK, ic.nt * kRows);
+          }
+#pragma unroll
+          for (int j = 0; j < SUB; ++j)
+            tma_load_2d(smem + S::X_OFF + s * S::XB + j * BN * 128, &maps.x[ic.p], &full[s], c * KC + j * 64,
+                        ic.mt * BN);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int g = 0, n_it = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++n_it) {
+        const ItemCoord ic = item_coord(P, it);
+        const int nch = (P.prob[ic.p].K + KC - 1) / KC;
+        const int buf = n_it & 1;
+        if (n_it >= 2 && !mbar_wait(&dempty[buf], ((n_it >> 1) & 1) ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + T::D_COL + buf * BN;
+        for (int c = 0; c < nch; ++c, ++g) {
+          const int s = g % STAGES, slot = g % kNA;
+          if (!mbar_wait(&full[s], (g / STAGES) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&afull[slot], (g / kNA) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t xaddr = smem_u32(smem + S::X_OFF + s * S::XB);
+#pragma unroll
+          for (int kk = 0; kk < KC / 16; ++kk) {
+            const uint64_t bdesc = smem_desc(xaddr + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024, 2);
+            mma_bf16_ts(d_tmem, tmem_base + slot * T::ACOLS + kk * 8, bdesc, IDESC, (c | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&aempty[slot]);
+          tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(&dfull[buf]);
+      }
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------ dequant warps: half h of every chunk
+    const int q = warp & 3;
+    const int h = (warp - 2) / 4;
+    const int r = q * 32 + lane;
+    const int lsel = (LUTREP > 1) ? (lane & (LUTREP - 1)) : 0;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    int g = 0, n_it = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++n_it) {
+      const ItemCoord ic = item_coord(P, it);
+      const PProblem& pr = P.prob[ic.p];
+      const int nb = pr.K / 64;                 // 64-element blocks per row
+      const int nch = (pr.K + KC - 1) / KC;
+      const int sb = n_it & 1;
+      const int64_t n = (int64_t)ic.nt * kRows + r;
+      const bool row_ok = n < pr.N;
+      if (!mbar_wait(&sfull[sb], (n_it >> 1) & 1, abort_flag)) break;
+      const uint8_t* sc = scbuf + sb * P.sc_bytes;
+      const float* s2s = s2buf + sb * kS2Max;
+      const int64_t g0 = ((int64_t)ic.nt * kRows * nb) / 256;  // NF4: first s2 group of the tile
+      const float off = (FMT == WQ_NF4) ? s2s[kS2Max - 1] : 0.0f;
+      for (int c = 0; c < nch; ++c, ++g) {
+        const int s = g % STAGES, slot = g % kNA;
+        // the 64-block this warp decodes (KC == 128), or the block holding its half (KC == 64)
+        const int blk = (KC == 128) ? 2 * c + h : c;
+        uint32_t sword = 0u;
+        if (row_ok && blk < nb) {
+          if (FMT == WQ_NF4) {
+            const int8_t qa = (int8_t)sc[r * nb + blk];
+            const float s2 = s2s[(n * nb + blk) / 256 - g0];
+            sword = __float_as_uint(__fadd_rn(__fmul_rn((float)qa, s2), off));
+          } else {
+            sword = *reinterpret_cast<const uint32_t*>(sc + 4 * (r * nb + blk));
+          }
+        }
+        if (!mbar_wait(&full[s], (g / STAGES) & 1, abort_flag)) { ok = false; break; }
+        if (g >= kNA && !mbar_wait(&aempty[slot], ((g / kNA) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        uint32_t v[NE / 2];
+        decode_span<FMT, NE, LUTREP>(sword, (KC == 128) ? 0 : h,
+                                     smem + S::W_OFF + s * S::WB + r * WCHUNK + h * (WCHUNK / 2), lut, lsel, v);
+        tmem_st_n(tmem_base + lane_base + slot * T::ACOLS + h * (NE / 2), v);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) { mbar_arrive(&afull[slot]); mbar_arrive(&empty[s]); }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[sb]);
+    }
+  } else if (warp < kScaleWarp) {
+    // ------------------------------------------------ epilogue warps
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    griddep_wait();
+    int n_it = 0;
+    for (int it = blockIdx.x; it < total; it += gridDim.x, ++n_it) {
+      const ItemCoord ic = item_coord(P, it);
+      const PProblem& pr = P.prob[ic.p];
+      const int buf = n_it & 1;
+      const int64_t n = (int64_t)ic.nt * kRows + r;
+      const bool row_ok = n < pr.N;
+      const float gsc = (FMT == WQ_NVFP4) ? *reinterpret_cast<const float*>(pr.scales + pr.lay.g_off) : 1.0f;
+      const float bval = (pr.bias && row_ok) ? bf16_bits_to_f32(pr.bias[n]) : 0.0f;
+      if (!mbar_wait(&dfull[buf], (n_it >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      const int m0 = ic.mt * BN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float acc[16];
+        tmem_ld16(tmem_base + lane_base + T::D_COL + buf * BN + c0, acc);
+        tc_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < pr.M) {
+              const float val = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
+              if (P.out_f32)
+                reinterpret_cast<float*>(pr.y)[(int64_t)m * pr.N + n] = val;
+              else
+                reinterpret_cast<__nv_bfloat16*>(pr.y)[(int64_t)m * pr.N + n] = __float2bfloat16_rn(val);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dempty[buf]);
+    }
+  } else {
+    // ------------------------------------------------ scale warp: one item ahead of the dequant warps,
+    // one bulk copy of the tile's scale slice (contiguous in the blob) into shared memory
+    int n_it = 0;
+    for (int it = blockIdx.x; it < total; it += gridDim.x, ++n_it) {
+      const ItemCoord ic = item_coord(P, it);
+      const PProblem& pr = P.prob[ic.p];
+      const int nb = pr.K / 64;
+      const int sb = n_it & 1;
+      if (n_it >= 2 && !mbar_wait(&sempty[sb], ((n_it >> 1) & 1) ^ 1, abort_flag)) break;
+      const int64_t n0 = (int64_t)ic.nt * kRows;
+      const int rows = (int)((pr.N - n0) < kRows ? (pr.N - n0) : kRows);
+      const int row_bytes = (FMT == WQ_NF4) ? nb : 4 * nb;
+      // 16-byte aligned source (n0 * row_bytes is a multiple of 16) and a size rounded up to 16:
+      // the scale regions of the blob are zero-padded to 16 bytes, so this stays inside it
+      const uint32_t bytes = (uint32_t)(((int64_t)rows * row_bytes + 15) / 16 * 16);
+      if (FMT == WQ_NF4) {
+        const int64_t b_lo = n0 * nb, b_hi = b_lo + (int64_t)rows * nb;  // absmax index range
+        const int64_t g0 = b_lo / 256, g1 = (b_hi - 1) / 256;
+        float* s2s = s2buf + sb * kS2Max;
+        const float* s2g = reinterpret_cast<const float*>(pr.scales + pr.lay.s2_off);
+        for (int64_t gi = g0 + lane; gi <= g1; gi += 32) s2s[gi - g0] = s2g[gi];
+        if (lane == 0) s2s[kS2Max - 1] = *reinterpret_cast<const float*>(pr.scales + pr.lay.offset_off);
+      }
+      if (lane == 0) {
+        uint64_t* bar = &sfull[sb];
+        mbar_arrive_expect_tx(bar, bytes);
+        const uint8_t* src = pr.scales + n0 * row_bytes;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                smem_u32(scbuf + sb * P.sc_bytes)),
+            "l"(src), "r"(bytes), "r"(smem_u32(bar))
+            : "memory");
+      } else {
+        mbar_arrive(&sfull[sb]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, T::ALLOC);
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
+  });
+  return n;
+}
+
+template <int BN, int STAGES, int FMT, int KC, int LUTREP>
+int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_static, cudaStream_t s) {
+  using S = PSmem<BN, STAGES, FMT, KC, LUTREP>;
+  auto kern = wq_tcp_kernel<BN, STAGES, FMT, KC, LUTREP>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::total(kMaxChunks));
+  });
+  if (attr_err != cudaSuccess) return WQ_ERR_CUDA;
+
+  // heavier items (longer K) first, so the round-robin over CTAs stays balanced
+  std::vector<int> order(count);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return probs[a].K > probs[b].K; });
+
+  static PMaps maps;    // host staging; copied into the launch's parameter buffer
+  static PParams P;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  P.nprob = count;
+  P.out_f32 = out_f32 ? 1 : 0;
+  P.weights_static = weights_static ? 1 : 0;
+  int items = 0;
+  for (int j = 0; j < count; ++j) {
+    const LinearArgs& a = probs[order[j]];
+    PProblem& pr = P.prob[j];
+    pr.scales = a.scales;
+    pr.bias = a.bias;
+    pr.y = a.y;
+    pr.M = (int)a.M;
+    pr.N = (int)a.N;
+    pr.K = (int)a.K;
+    pr.ntiles = (int)((a.N + kRows - 1) / kRows);
+    pr.mtiles = (int)((a.M + BN - 1) / BN);
+    pr.item_begin = items;
+    pr.lay = scales_layout(FMT, a.N, a.K);
+    items += pr.ntiles * pr.mtiles;
+    const uint64_t wrow = (uint64_t)(FMT == WQ_Q8_0 ? a.K : a.K / 2);
+    if (!encode_tmap_2d(&maps.x[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M,
+                        (uint64_t)a.K * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+      return WQ_ERR_CUDA;
+    if (!encode_tmap_2d(&maps.w[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, wrow, (uint64_t)a.N, wrow,
+                        Fmt<FMT>::WB * (KC / 64), kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return WQ_ERR_CUDA;
+  }
+  P.total_items = items;
+  if (items == 0) return WQ_OK;
+  int max_blocks = 1;
+  for (int j = 0; j < count; ++j) max_blocks = std::max(max_blocks, P.prob[j].K / 64);
+  P.sc_bytes = S::sc_bytes(max_blocks);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min(items, num_sms()), 1, 1);
+  cfg.blockDim = dim3(kPThreads, 1, 1);
+  cfg.dynamicSmemBytes = S::total(max_blocks);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  int na = 0;
+  if (weights_static) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    na = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, P);
+  count_launch();
+  return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+// decode: 128-element chunks, lane-replicated LUT; GEMM: 64-element chunks, compact LUT
+constexpr int decode_stages(int fmt) { return fmt == WQ_Q8_0 ? 5 : 8; }
+constexpr int kGemmStagesP = 4;
+
+template <int FMT>
+int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_static, cudaStream_t s) {
+  int64_t maxM = 0;
+  for (int i = 0; i < count; ++i) maxM = std::max(maxM, probs[i].M);
+  if (maxM <= 16)
+    return launch_tcp<16, decode_stages(FMT), FMT, 128, 16>(probs, count, out_f32, weights_static, s);
+  return launch_tcp<128, kGemmStagesP, FMT, 64, 1>(probs, count, out_f32, weights_static, s);
+}
+
+}  // namespace
+
+bool tcp_eligible(const LinearArgs& a) {
+  if (a.fmt != WQ_NF4 && a.fmt != WQ_NVFP4 && a.fmt != WQ_Q4_0 && a.fmt != WQ_Q8_0) return false;
+  if (a.K % kKS != 0 || a.K < kKS || a.K > (int64_t)kKS * kMaxChunks) return false;
+  if (a.M > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF) return false;
+  return ((uintptr_t)a.x & 15u) == 0;
+}
+
+int linear_tcp(const LinearArgs* probs, int count, cudaStream_t s) {
+  if (count <= 0) return WQ_OK;
+  const bool out_f32 = probs[0].out_f32, ws = probs[0].weights_static;
+  switch (probs[0].fmt) {
+    case WQ_NF4: return dispatch_p<WQ_NF4>(probs, count, out_f32, ws, s);
+    case WQ_NVFP4: return dispatch_p<WQ_NVFP4>(probs, count, out_f32, ws, s);
+    case WQ_Q4_0: return dispatch_p<WQ_Q4_0>(probs, count, out_f32, ws, s);
+    case WQ_Q8_0: return dispatch_p<WQ_Q8_0>(probs, count, out_f32, ws, s);
+    default: return WQ_ERR_FMT;
+  }
+}
+
+int take_status_tcp() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return WQ_ERR_CUDA;
+  cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace wq

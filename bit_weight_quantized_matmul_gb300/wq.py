@@ -31,6 +31,14 @@ class wq_act_nvfp4(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("g", ctypes.c_void_p)]
 
 
+class wq_problem(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+WQ_GROUP_MAX = 48
+
 _P, _I64, _I, _U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint
 _SIGS = {
     "wq_packed_bytes": (ctypes.c_size_t, [_I, _I64, _I64]),
@@ -43,6 +51,7 @@ _SIGS = {
     "wq_quant_act_nvfp4": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _P]),
     "wq_linear": (_I, [_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
     "wq_linear_ex": (_I, [_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _U, _P]),
+    "wq_linear_grouped": (_I, [_P, _I, _I, _U, _P]),
     "wq_last_device_status": (_I, []),
     "wq_status_string": (ctypes.c_char_p, [_I]),
     "wq_kernel_launches": (ctypes.c_uint64, []),
@@ -159,6 +168,18 @@ def linear(x, packed, scales, fmt, N, K, bias=None, out_f32=False, weights_stati
     dev = x[0].device if _fmt(fmt) == WQ_NVFP4_W4A4 else x.device
     y = torch.empty((M, N), dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
     return linear_into(y, x, packed, scales, fmt, N, K, bias, out_f32, weights_static, force_simt, stream)
+
+
+def linear_grouped(problems, fmt, out_f32=False, weights_static=False, stream=None):
+    """Independent Linears of one format in one launch.  ``problems`` is a list of
+    (y, x, packed, scales, N, K, bias) tuples; each y [M, N] is written in place."""
+    arr = (wq_problem * len(problems))()
+    for i, (y, x, packed, scales, N, K, bias) in enumerate(problems):
+        arr[i] = wq_problem(x.data_ptr(), packed.data_ptr(), scales.data_ptr(),
+                            None if bias is None else bias.data_ptr(), y.data_ptr(), x.shape[0], N, K)
+    flags = (WQ_FLAG_OUT_F32 if out_f32 else 0) | (WQ_FLAG_WEIGHTS_STATIC if weights_static else 0)
+    _check("wq_linear_grouped", lib.wq_linear_grouped(ctypes.cast(arr, ctypes.c_void_p), len(problems),
+                                                      _fmt(fmt), flags, _stream(stream)))
 
 
 def last_device_status():

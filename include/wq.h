@@ -79,7 +79,7 @@ typedef struct wq_act_nvfp4 {
  *   scales  NF4:   int8 absmax codes [N*K/64] | zero pad to 16 B |
  *                  fp32 second-level scale s2 [ceil(N*K/64 / 256)] | fp32 offset
  *           NVFP4: E4M3 block scales [N, K/16] row-major | zero pad to 16 B | fp32 g
- *           q4_0, q8_0: fp16 d [N*K/32]
+ *           q4_0, q8_0: fp16 d [N*K/32] | zero pad to 16 B
  * Size rules: NF4 K % 64 == 0; NVFP4 K % 32 == 0; q4_0 / q8_0 K % 32 == 0.   */
 size_t wq_packed_bytes(int fmt, int64_t N, int64_t K);
 size_t wq_scales_bytes(int fmt, int64_t N, int64_t K);
@@ -133,9 +133,9 @@ int wq_quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_i
  *   bias   bf16 [N] or NULL
  *   y      bf16 [M, N]
  * M == 0 is a no-op.  Dispatch: M <= 16 runs the decode path (tensor-core
- * GEMV, split-K over a thread-block cluster); larger M runs the tensor-core
- * GEMM; shapes outside the fast paths' rules (see DESIGN) run a CUDA-core
- * kernel with the same arithmetic.                                              */
+ * GEMV, split-K over a thread-block cluster); larger M runs the persistent
+ * tensor-core GEMM; K not a multiple of 64 runs a CUDA-core kernel with the
+ * same per-weight decode.                                                       */
 int wq_linear(const void* x, const void* packed, const void* scales, int fmt,
               int64_t M, int64_t N, int64_t K, const uint16_t* bias, void* y, void* stream);
 
@@ -156,6 +156,26 @@ enum {
 int wq_linear_ex(const void* x, const void* packed, const void* scales, int fmt,
                  int64_t M, int64_t N, int64_t K, const uint16_t* bias, void* y,
                  unsigned flags, void* stream);
+
+/* ---------------------------------------------------------------- grouped
+ * Several independent Linears of ONE format in one launch (the fused Q/K/V
+ * projection of PR "Run quantized Whisper on the fused Metal decode path",
+ * "Summary", generalised to any set of Linears whose inputs are ready).  Each
+ * problem has the meaning of one wq_linear call (same layouts and rules);
+ * outputs must not overlap.  `problems` is a HOST array of `count` entries,
+ * 1 <= count <= WQ_GROUP_MAX; WQ_NVFP4_W4A4 is not accepted (WQ_ERR_FMT).
+ * flags: WQ_FLAG_OUT_F32 / WQ_FLAG_WEIGHTS_STATIC apply to every problem.     */
+#define WQ_GROUP_MAX 48
+typedef struct wq_problem {
+  const void* x;          /* bf16 [M, K]          */
+  const void* packed;     /* packed weight        */
+  const void* scales;     /* its scales blob      */
+  const uint16_t* bias;   /* bf16 [N] or NULL     */
+  void* y;                /* bf16 (or fp32) [M, N] */
+  int64_t M, N, K;
+} wq_problem;
+
+int wq_linear_grouped(const wq_problem* problems, int count, int fmt, unsigned flags, void* stream);
 
 /* ---------------------------------------------------------------- status
  * wq_last_device_status: synchronises the current device, returns and clears

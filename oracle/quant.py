@@ -235,7 +235,7 @@ def to_blobs(p):
             q8_0: one int8 per element.
     scales: nf4:   int8 absmax codes [N*K/64] | zero pad to 16 B | fp32 s2 [groups] | fp32 offset
             nvfp4: E4M3 bytes [N, K/16] row-major | zero pad to 16 B | fp32 g
-            q4_0 / q8_0: fp16 d [N*K/32]
+            q4_0 / q8_0: fp16 d [N*K/32] | zero pad to 16 B
     """
     fmt = p["fmt"]
     if fmt in ("nf4", "nvfp4", "q4_0"):
@@ -250,5 +250,6 @@ def to_blobs(p):
         s = np.asarray(p["scales"], np.uint8).tobytes()
         scales = s + b"\0" * (_align16(len(s)) - len(s)) + np.float32(p["g"]).tobytes()
     else:
-        scales = np.asarray(p["d"], np.float16).tobytes()
+        d = np.asarray(p["d"], np.float16).tobytes()
+        scales = d + b"\0" * (_align16(len(d)) - len(d))
     return packed, scales

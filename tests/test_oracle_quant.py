@@ -99,7 +99,7 @@ def test_q4_0_hand_worked_example():
     packed, scales = Q.to_blobs(p)
     assert packed[:5] == bytes(int(b, 16) for b in g["packed0"][0])
     assert packed[16:19] == bytes(int(b, 16) for b in g["packed1"][0])
-    assert scales == bytes([0x00, 0x38, 0x00, 0xB4])
+    assert scales == bytes([0x00, 0x38, 0x00, 0xB4]) + b"\0" * 12
 
 
 def test_q4_0_decode_identity_all_codes():
