@@ -139,6 +139,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return false;
 }
 
+// Warp-wide bounded wait: lane i waits on bar[i] with parity par[i] when active[i]; one
+// try_wait instruction per poll covers every lane's barrier, so independent waits
+// overlap instead of paying the barrier latency one after another.  Returns false
+// (and raises *abort) on timeout.  Must be called by all 32 lanes.
+__device__ __forceinline__ bool mbar_wait_lanes(uint64_t* bar, uint32_t parity, bool active,
+                                                volatile int* abort) {
+  bool done = !active;
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (!done) done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xFFFFFFFFu, done)) return true;
+    if ((i & 1023u) == 1023u && *abort) return false;
+  }
+  set_status(WQ_STATUS_TIMEOUT);
+  *abort = 1;
+  return false;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1) {

@@ -221,5 +221,62 @@ __device__ __forceinline__ void decode_span(uint32_t sword, int part, const uint
 __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&v)[16]) { tmem_st16(taddr, v); }
 __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&v)[32]) { tmem_st32(taddr, v); }
 
+// Byte -> packed bf16 pair (value of the low nibble in the low half).  NF4 values are
+// rounded to bf16 here; q4_0's (q - 8) and NVFP4's E2M1 values are exact in bf16.
+template <int FMT>
+__device__ __forceinline__ uint32_t nibble_pair_bf16(uint32_t byte) {
+  return pack_bf16x2(nibble_value<FMT>(byte & 15u), nibble_value<FMT>(byte >> 4));
+}
+
+__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 r = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Decode NE elements of one 64-element block with a bf16-pair table (LUTREP copies,
+// `lsel` = this lane's copy).  SCALED: multiply each pair by the block's NVFP4 E4M3
+// scale in bf16 (exact: an E2M1 value times an E4M3 value has at most 5 significant
+// bits).  Unscaled (the per-block scale is applied to the MMA partial sums
+// afterwards): NF4 codebook values in bf16, q4_0 (q - 8), q8_0 q -- the last two exact.
+template <int FMT, int NE, int LUTREP, bool SCALED>
+__device__ __forceinline__ void decode_span_bf16(uint32_t sword, int part, const uint8_t* wsrc,
+                                                 const uint32_t* lut, int lsel, uint32_t (&out)[NE / 2]) {
+  static_assert(NE == 32 || NE == 64, "span");
+  if (FMT == WQ_Q8_0) {
+#pragma unroll
+    for (int q = 0; q < NE / 16; ++q) {
+      const uint4 v = reinterpret_cast<const uint4*>(wsrc)[q];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        out[q * 8 + j * 2] = pack_bf16x2((float)(int8_t)(u[j] & 0xFF), (float)(int8_t)((u[j] >> 8) & 0xFF));
+        out[q * 8 + j * 2 + 1] = pack_bf16x2((float)(int8_t)((u[j] >> 16) & 0xFF), (float)(int8_t)(u[j] >> 24));
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int q = 0; q < NE / 32; ++q) {
+    const uint4 v = reinterpret_cast<const uint4*>(wsrc)[q];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t spair = 0u;
+      if (SCALED) {
+        const int e0 = part * NE + q * 32 + j * 8;
+        const uint32_t sb = __float_as_uint(e4m3_to_f32((sword >> (8 * (e0 / 16))) & 0xFFu)) >> 16;
+        spair = sb | (sb << 16);  // E4M3 values are exact in bf16
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t pair = lut[((u[j] >> (8 * b)) & 0xFFu) * LUTREP + lsel];
+        out[q * 16 + j * 4 + b] = SCALED ? hmul2_bf16(pair, spair) : pair;
+      }
+    }
+  }
+}
+
 }  // namespace tc
 }  // namespace wq

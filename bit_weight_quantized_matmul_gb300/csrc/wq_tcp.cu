@@ -42,11 +42,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kNA = 4;            // TMEM A ring slots
+constexpr int kMaxItems = 4096;   // items a launch can schedule with an explicit per-CTA list
 constexpr int kDeqWarps = 8;      // two per TMEM lane quarter, each decoding half of a chunk
 constexpr int kEpiWarp0 = 2 + kDeqWarps;
 constexpr int kScaleWarp = kEpiWarp0 + 4;
 constexpr int kPThreads = (kScaleWarp + 1) * 32;  // 15 warps
+constexpr int kMaxCtas = 160;     // persistent grid: one CTA per SM (152 on GB300)
 constexpr int kMaxChunks = 80;    // 64-element blocks per row: K <= 5120 on this path
 constexpr int kS2Max = 48;        // NF4: s2 values a tile can touch (128 * 80 / 256 + 2) + offset
 
@@ -62,17 +63,48 @@ struct PProblem {
 
 struct PParams {
   int nprob, total_items, out_f32, weights_static;
-  int sc_bytes;  // bytes per scale buffer (max over the problems)
+  int sc_bytes;    // bytes per scale buffer (max over the problems)
+  int use_list;    // 1: CTA b runs items list[begin[b] .. begin[b+1]); 0: items b, b + grid, ...
   PProblem prob[kGroupMax];
+  uint16_t begin[kMaxCtas + 1];
+  uint16_t list[kMaxItems];
+};
+
+// The items a CTA runs, in order.
+struct ItemIter {
+  int pos, end, step;
+  bool list;
+  __device__ ItemIter(const PParams& P) {
+    list = P.use_list != 0;
+    if (list) { pos = P.begin[blockIdx.x]; end = P.begin[blockIdx.x + 1]; step = 1; }
+    else { pos = blockIdx.x; end = P.total_items; step = gridDim.x; }
+  }
+  __device__ bool more() const { return pos < end; }
+  __device__ int item(const PParams& P) const { return list ? (int)P.list[pos] : pos; }
+  __device__ void next() { pos += step; }
 };
 
 struct PMaps {
   CUtensorMap w[kGroupMax];
   CUtensorMap x[kGroupMax];
 };
+static_assert(sizeof(PMaps) + sizeof(PParams) <= 32000, "kernel parameter space");
+
+template <int KC>
+constexpr int a_slots() { return KC == 256 ? 2 : 4; }  // TMEM A ring slots
+
+// Where the per-block weight scales are applied:
+//   kScaleF32   dequant warps multiply each code's value by its block scale in fp32
+//               (byte -> float pair table) -- the encoder GEMM path
+//   kScaleBF16  dequant warps multiply in bf16 pairs, exact for NVFP4 only
+//               (byte -> bf16 pair table) -- NVFP4 decode
+//   kScaleFold  dequant warps emit unscaled values (byte -> bf16 pair table); every
+//               MMA K step of a scale block writes its own TMEM partial and four fold
+//               warps add  scale * partial  in fp32 -- NF4 / q4_0 / q8_0 decode
+enum { kScaleF32 = 0, kScaleBF16 = 1, kScaleFold = 2 };
 
 // KC: K elements per pipeline chunk (64 or 128: one or two 128-byte swizzle rows of x)
-template <int BN, int STAGES, int FMT, int KC, int LUTREP>
+template <int BN, int STAGES, int FMT, int KC, int LUTREP, int MODE>
 struct PSmem {
   static constexpr int SUB = KC / 64;
   static constexpr int XB = SUB * BN * 128;
@@ -80,9 +112,9 @@ struct PSmem {
   static constexpr int X_OFF = 0;
   static constexpr int W_OFF = X_OFF + STAGES * XB;
   static constexpr int LUT_OFF = W_OFF + STAGES * WB;
-  static constexpr int LUT_BYTES = (FMT == WQ_Q8_0) ? 0 : 256 * 8 * LUTREP;
+  static constexpr int LUT_BYTES = (FMT == WQ_Q8_0) ? 0 : 256 * (MODE == kScaleF32 ? 8 : 4) * LUTREP;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
-  static constexpr int NBAR = 2 * STAGES + 2 * kNA + 8;
+  static constexpr int NBAR = 2 * STAGES + 2 * a_slots<KC>() + 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int S2_OFF = (MISC_OFF + 16 + 15) / 16 * 16;               // [2][kS2Max] NF4 s2 + offset
   static constexpr int SC_OFF = (S2_OFF + 2 * kS2Max * 4 + 127) / 128 * 128;  // [2] raw scale slices
@@ -94,11 +126,17 @@ struct PSmem {
   static_assert(total(kMaxChunks) <= 227 * 1024, "shared memory budget");
 };
 
-template <int BN, int KC>
+template <int FMT>
+constexpr int scale_groups_per_128() { return FMT == WQ_NF4 ? 2 : FMT == WQ_NVFP4 ? 8 : 4; }
+
+template <int BN, int KC, int FMT, int MODE>
 struct PTmem {
+  static constexpr int NA = a_slots<KC>();
   static constexpr int ACOLS = KC / 2;  // 32-bit columns per A slot (bf16 pairs)
-  static constexpr int D_COL = kNA * ACOLS;
-  static constexpr int USED = D_COL + 2 * BN;
+  static constexpr int D_COL = NA * ACOLS;
+  // kScaleFold: a double-buffered ring of per-scale-block partial tiles instead of D
+  static constexpr int G = scale_groups_per_128<FMT>() * KC / 128;
+  static constexpr int USED = D_COL + 2 * BN * (MODE == kScaleFold ? G : 1);
   static constexpr int ALLOC = USED <= 256 ? 256 : 512;
   static_assert(USED <= 512, "TMEM budget");
 };
@@ -115,11 +153,16 @@ __device__ __forceinline__ ItemCoord item_coord(const PParams& P, int i) {
   return ItemCoord{p, local % nt_count, local / nt_count};
 }
 
-template <int BN, int STAGES, int FMT, int KC, int LUTREP>
+template <int BN, int STAGES, int FMT, int KC, int LUTREP, int MODE>
 __global__ void __launch_bounds__(kPThreads, 1)
     wq_tcp_kernel(const __grid_constant__ PMaps maps, const __grid_constant__ PParams P) {
-  using S = PSmem<BN, STAGES, FMT, KC, LUTREP>;
-  using T = PTmem<BN, KC>;
+  using S = PSmem<BN, STAGES, FMT, KC, LUTREP, MODE>;
+  using T = PTmem<BN, KC, FMT, MODE>;
+  static_assert(MODE != kScaleFold || (BN == 16 && FMT != WQ_NVFP4), "fold mode: decode tiles");
+  static_assert(MODE != kScaleBF16 || FMT == WQ_NVFP4, "bf16 scaling is exact for NVFP4 only");
+  constexpr bool FOLD = MODE == kScaleFold;
+  constexpr int kNA = T::NA;
+  constexpr int SCALE_CONSUMERS = FOLD ? 4 : kDeqWarps;
   constexpr int SUB = S::SUB;
   constexpr int NE = KC / 2;  // elements of a row each dequant warp decodes per chunk
   constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
@@ -140,6 +183,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
   float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
+  uint32_t* lut32 = reinterpret_cast<uint32_t*>(smem + S::LUT_OFF);
   uint8_t* scbuf = smem + S::SC_OFF;
   float* s2buf = reinterpret_cast<float*>(smem + S::S2_OFF);
 
@@ -149,10 +193,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1 + kDeqWarps); }
     for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], 1); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&dfull[i], 1);
-      mbar_init(&dempty[i], 4);
+      mbar_init(&dfull[i], 1);   // kScaleFold: a partial-tile slot is full
+      mbar_init(&dempty[i], 4);  // kScaleFold: a partial-tile slot was folded
       mbar_init(&sfull[i], 32);
-      mbar_init(&sempty[i], kDeqWarps);
+      mbar_init(&sempty[i], SCALE_CONSUMERS);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -160,7 +204,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (FMT != WQ_Q8_0) {
     for (int i = threadIdx.x; i < 256 * LUTREP; i += kPThreads) {
       const uint32_t b = (uint32_t)(i / LUTREP);
-      lut[i] = make_float2(nibble_value<FMT>(b & 15u), nibble_value<FMT>(b >> 4));
+      if (MODE == kScaleF32)
+        lut[i] = make_float2(nibble_value<FMT>(b & 15u), nibble_value<FMT>(b >> 4));
+      else
+        lut32[i] = nibble_pair_bf16<FMT>(b);
     }
   }
   if (warp == 1) tmem_alloc(tmem_slot, T::ALLOC);
@@ -182,8 +229,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int pre = 0;
       if (P.weights_static) {
         int g = 0;
-        for (int it = blockIdx.x; it < total && g < STAGES; it += gridDim.x) {
-          const ItemCoord ic = item_coord(P, it);
+        for (ItemIter ii(P); ii.more() && g < STAGES; ii.next()) {
+          const ItemCoord ic = item_coord(P, ii.item(P));
           const int nch = (P.prob[ic.p].K + KC - 1) / KC;
           for (int c = 0; c < nch && g < STAGES; ++c, ++g) {
             mbar_arrive_expect_tx(&full[g], STAGE_TX);
@@ -195,8 +242,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       griddep_wait();
       int g = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-        const ItemCoord ic = item_coord(P, it);
+      for (ItemIter ii(P); ii.more() && ok; ii.next()) {
+        const ItemCoord ic = item_coord(P, ii.item(P));
         const int nch = (P.prob[ic.p].K + KC - 1) / KC;
         for (int c = 0; c < nch; ++c, ++g) {
           const int s = g % STAGES;
@@ -213,32 +260,50 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------ MMA issuer (whole warp waits, lane 0 issues)
+    // A chunk's x tile is in shared memory once its A slot is full: every dequant warp waited
+    // for the stage's TMA transaction before it arrived on afull.
+    {
       int g = 0, n_it = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++n_it) {
-        const ItemCoord ic = item_coord(P, it);
+      for (ItemIter ii(P); ii.more() && ok; ii.next(), ++n_it) {
+        const ItemCoord ic = item_coord(P, ii.item(P));
         const int nch = (P.prob[ic.p].K + KC - 1) / KC;
         const int buf = n_it & 1;
-        if (n_it >= 2 && !mbar_wait(&dempty[buf], ((n_it >> 1) & 1) ^ 1, abort_flag)) break;
+        if (!FOLD && !mbar_wait_lanes(&dempty[buf], ((n_it >> 1) & 1) ^ 1, lane == 0 && n_it >= 2, abort_flag))
+          break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + T::D_COL + buf * BN;
         for (int c = 0; c < nch; ++c, ++g) {
           const int s = g % STAGES, slot = g % kNA;
-          if (!mbar_wait(&full[s], (g / STAGES) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&afull[slot], (g / kNA) & 1, abort_flag)) { ok = false; break; }
+          // lane 0: the A slot; lane 1 (fold mode): the partial-tile slot
+          uint64_t* wb = (lane == 0) ? &afull[slot] : &dempty[g & 1];
+          const uint32_t wp = (lane == 0) ? ((g / kNA) & 1) : (((g >> 1) & 1) ^ 1);
+          const bool act = (lane == 0) || (FOLD && lane == 1 && g >= 2);
+          if (!mbar_wait_lanes(wb, wp, act, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t xaddr = smem_u32(smem + S::X_OFF + s * S::XB);
+          if (lane == 0) {
+            const uint32_t xaddr = smem_u32(smem + S::X_OFF + s * S::XB);
 #pragma unroll
-          for (int kk = 0; kk < KC / 16; ++kk) {
-            const uint64_t bdesc = smem_desc(xaddr + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024, 2);
-            mma_bf16_ts(d_tmem, tmem_base + slot * T::ACOLS + kk * 8, bdesc, IDESC, (c | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < KC / 16; ++kk) {
+              const uint64_t bdesc = smem_desc(xaddr + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024, 2);
+              const uint32_t a_tmem = tmem_base + slot * T::ACOLS + kk * 8;
+              if (FOLD) {
+                constexpr int KPG = (KC / 16) / T::G;  // MMA K steps per scale block
+                const uint32_t p_tmem = tmem_base + T::D_COL + ((g & 1) * T::G + kk / KPG) * BN;
+                mma_bf16_ts(p_tmem, a_tmem, bdesc, IDESC, (kk % KPG) != 0 ? 1u : 0u);
+              } else {
+                mma_bf16_ts(d_tmem, a_tmem, bdesc, IDESC, (c | kk) != 0 ? 1u : 0u);
+              }
+            }
+            tc_commit(&aempty[slot]);
+            tc_commit(&empty[s]);
+            if (FOLD) tc_commit(&dfull[g & 1]);
           }
-          tc_commit(&aempty[slot]);
-          tc_commit(&empty[s]);
+          __syncwarp();
         }
-        if (ok) tc_commit(&dfull[buf]);
+        if (ok && !FOLD && lane == 0) tc_commit(&dfull[buf]);
+        __syncwarp();
       }
     }
   } else if (warp < kEpiWarp0) {
@@ -250,46 +315,60 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int g = 0, n_it = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++n_it) {
-      const ItemCoord ic = item_coord(P, it);
+    for (ItemIter ii(P); ii.more() && ok; ii.next(), ++n_it) {
+      const ItemCoord ic = item_coord(P, ii.item(P));
       const PProblem& pr = P.prob[ic.p];
       const int nb = pr.K / 64;                 // 64-element blocks per row
       const int nch = (pr.K + KC - 1) / KC;
       const int sb = n_it & 1;
       const int64_t n = (int64_t)ic.nt * kRows + r;
       const bool row_ok = n < pr.N;
-      if (!mbar_wait(&sfull[sb], (n_it >> 1) & 1, abort_flag)) break;
+      if (!FOLD && !mbar_wait(&sfull[sb], (n_it >> 1) & 1, abort_flag)) break;
       const uint8_t* sc = scbuf + sb * P.sc_bytes;
       const float* s2s = s2buf + sb * kS2Max;
       const int64_t g0 = ((int64_t)ic.nt * kRows * nb) / 256;  // NF4: first s2 group of the tile
-      const float off = (FMT == WQ_NF4) ? s2s[kS2Max - 1] : 0.0f;
+      const float off = (FMT == WQ_NF4 && !FOLD) ? s2s[kS2Max - 1] : 0.0f;
       for (int c = 0; c < nch; ++c, ++g) {
         const int s = g % STAGES, slot = g % kNA;
-        // the 64-block this warp decodes (KC == 128), or the block holding its half (KC == 64)
-        const int blk = (KC == 128) ? 2 * c + h : c;
-        uint32_t sword = 0u;
-        if (row_ok && blk < nb) {
-          if (FMT == WQ_NF4) {
-            const int8_t qa = (int8_t)sc[r * nb + blk];
-            const float s2 = s2s[(n * nb + blk) / 256 - g0];
-            sword = __float_as_uint(__fadd_rn(__fmul_rn((float)qa, s2), off));
-          } else {
-            sword = *reinterpret_cast<const uint32_t*>(sc + 4 * (r * nb + blk));
+        constexpr int NBW = (KC >= 128) ? NE / 64 : 1;  // 64-blocks this warp decodes per chunk
+        uint32_t sword[NBW];
+#pragma unroll
+        for (int bb = 0; bb < NBW; ++bb) {
+          // the 64-block this warp decodes (KC >= 128), or the block holding its half (KC == 64)
+          const int blk = (KC >= 128) ? (KC / 64) * c + NBW * h + bb : c;
+          sword[bb] = 0u;
+          if (!FOLD && row_ok && blk < nb) {
+            if (FMT == WQ_NF4) {
+              const int8_t qa = (int8_t)sc[r * nb + blk];
+              const float s2 = s2s[(n * nb + blk) / 256 - g0];
+              sword[bb] = __float_as_uint(__fadd_rn(__fmul_rn((float)qa, s2), off));
+            } else {
+              sword[bb] = *reinterpret_cast<const uint32_t*>(sc + 4 * (r * nb + blk));
+            }
           }
         }
         if (!mbar_wait(&full[s], (g / STAGES) & 1, abort_flag)) { ok = false; break; }
         if (g >= kNA && !mbar_wait(&aempty[slot], ((g / kNA) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        uint32_t v[NE / 2];
-        decode_span<FMT, NE, LUTREP>(sword, (KC == 128) ? 0 : h,
-                                     smem + S::W_OFF + s * S::WB + r * WCHUNK + h * (WCHUNK / 2), lut, lsel, v);
-        tmem_st_n(tmem_base + lane_base + slot * T::ACOLS + h * (NE / 2), v);
+        const uint8_t* wsrc = smem + S::W_OFF + s * S::WB + r * WCHUNK + h * (WCHUNK / 2);
+        constexpr int NES = NE / NBW;  // elements per decode call (32 or 64)
+#pragma unroll
+        for (int bb = 0; bb < NBW; ++bb) {
+          uint32_t v[NES / 2];
+          const int part = (KC == 64) ? h : 0;
+          const uint8_t* src = wsrc + bb * (WCHUNK / (2 * NBW));
+          if (MODE == kScaleF32)
+            decode_span<FMT, NES, LUTREP>(sword[bb], part, src, lut, lsel, v);
+          else
+            decode_span_bf16<FMT, NES, LUTREP, MODE == kScaleBF16>(sword[bb], part, src, lut32, lsel, v);
+          tmem_st_n(tmem_base + lane_base + slot * T::ACOLS + h * (NE / 2) + bb * (NES / 2), v);
+        }
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) { mbar_arrive(&afull[slot]); mbar_arrive(&empty[s]); }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sempty[sb]);
+      if (!FOLD && lane == 0) mbar_arrive(&sempty[sb]);
     }
   } else if (warp < kScaleWarp) {
     // ------------------------------------------------ epilogue warps
@@ -297,18 +376,83 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int r = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     griddep_wait();
-    int n_it = 0;
-    for (int it = blockIdx.x; it < total; it += gridDim.x, ++n_it) {
-      const ItemCoord ic = item_coord(P, it);
+    int n_it = 0, g = 0;
+    for (ItemIter ii(P); ii.more(); ii.next(), ++n_it) {
+      const ItemCoord ic = item_coord(P, ii.item(P));
       const PProblem& pr = P.prob[ic.p];
       const int buf = n_it & 1;
       const int64_t n = (int64_t)ic.nt * kRows + r;
       const bool row_ok = n < pr.N;
       const float gsc = (FMT == WQ_NVFP4) ? *reinterpret_cast<const float*>(pr.scales + pr.lay.g_off) : 1.0f;
       const float bval = (pr.bias && row_ok) ? bf16_bits_to_f32(pr.bias[n]) : 0.0f;
+      const int m0 = ic.mt * BN;
+      if (FOLD) {
+        // fold the per-scale-block partial tiles of every chunk: acc += scale * partial
+        const int nb = pr.K / 64;
+        const int nch = (pr.K + KC - 1) / KC;
+        const int sb = n_it & 1;
+        if (!mbar_wait(&sfull[sb], (n_it >> 1) & 1, abort_flag)) break;
+        const uint8_t* sc = scbuf + sb * P.sc_bytes;
+        const float* s2s = s2buf + sb * kS2Max;
+        const int64_t g0 = ((int64_t)ic.nt * kRows * nb) / 256;
+        const float off = (FMT == WQ_NF4) ? s2s[kS2Max - 1] : 0.0f;
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+        bool ok = true;
+        for (int c = 0; c < nch; ++c, ++g) {
+          // block scales of this row for the chunk's scale blocks (0 past the end of K)
+          float sg[T::G];
+#pragma unroll
+          for (int grp = 0; grp < T::G; ++grp) {
+            float sv = 0.0f;
+            if (FMT == WQ_NF4) {
+              const int blk = c * T::G + grp;  // 64-blocks
+              if (row_ok && blk < nb) {
+                const float s2 = s2s[(n * nb + blk) / 256 - g0];
+                sv = __fadd_rn(__fmul_rn((float)(int8_t)sc[r * nb + blk], s2), off);
+              }
+            } else {  // q4_0 / q8_0: 32-blocks, fp16 d
+              const int j32 = c * T::G + grp;
+              if (row_ok && j32 < 2 * nb)
+                sv = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(sc + 4 * r * nb + 2 * j32));
+            }
+            sg[grp] = sv;
+          }
+          if (!mbar_wait(&dfull[g & 1], (g >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int grp = 0; grp < T::G; ++grp) {
+            float pt[16];
+            tmem_ld16(tmem_base + lane_base + T::D_COL + ((g & 1) * T::G + grp) * BN, pt);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = fmaf(sg[grp], pt[j], acc[j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&dempty[g & 1]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[sb]);
+        if (!ok) break;
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + j;
+            if (m < pr.M) {
+              const float val = __fadd_rn(acc[j], bval);
+              if (P.out_f32)
+                reinterpret_cast<float*>(pr.y)[(int64_t)m * pr.N + n] = val;
+              else
+                reinterpret_cast<__nv_bfloat16*>(pr.y)[(int64_t)m * pr.N + n] = __float2bfloat16_rn(val);
+            }
+          }
+        }
+        continue;
+      }
       if (!mbar_wait(&dfull[buf], (n_it >> 1) & 1, abort_flag)) break;
       tc_fence_after();
-      const int m0 = ic.mt * BN;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float acc[16];
@@ -336,8 +480,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ------------------------------------------------ scale warp: one item ahead of the dequant warps,
     // one bulk copy of the tile's scale slice (contiguous in the blob) into shared memory
     int n_it = 0;
-    for (int it = blockIdx.x; it < total; it += gridDim.x, ++n_it) {
-      const ItemCoord ic = item_coord(P, it);
+    for (ItemIter ii(P); ii.more(); ii.next(), ++n_it) {
+      const ItemCoord ic = item_coord(P, ii.item(P));
       const PProblem& pr = P.prob[ic.p];
       const int nb = pr.K / 64;
       const int sb = n_it & 1;
@@ -391,10 +535,10 @@ int num_sms() {
   return n;
 }
 
-template <int BN, int STAGES, int FMT, int KC, int LUTREP>
+template <int BN, int STAGES, int FMT, int KC, int LUTREP, int MODE>
 int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_static, cudaStream_t s) {
-  using S = PSmem<BN, STAGES, FMT, KC, LUTREP>;
-  auto kern = wq_tcp_kernel<BN, STAGES, FMT, KC, LUTREP>;
+  using S = PSmem<BN, STAGES, FMT, KC, LUTREP, MODE>;
+  auto kern = wq_tcp_kernel<BN, STAGES, FMT, KC, LUTREP, MODE>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -439,12 +583,43 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   }
   P.total_items = items;
   if (items == 0) return WQ_OK;
+  const int grid = std::min(std::min(items, num_sms()), kMaxCtas);
+  // longest-processing-time-first assignment of items to CTAs (cost = K chunks + a fixed
+  // per-item overhead); items are visited heaviest first, each to the least-loaded CTA
+  P.use_list = items <= kMaxItems ? 1 : 0;
+  if (P.use_list) {
+    std::vector<int> order_items(items);
+    std::vector<int> cost(items);
+    for (int j = 0; j < count; ++j)
+      for (int i = 0; i < P.prob[j].ntiles * P.prob[j].mtiles; ++i)
+        cost[P.prob[j].item_begin + i] = (P.prob[j].K + KC - 1) / KC + 2;
+    std::iota(order_items.begin(), order_items.end(), 0);
+    std::stable_sort(order_items.begin(), order_items.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+    std::vector<std::vector<int>> bins(grid);
+    std::vector<std::pair<long, int>> heap;  // (load, cta), min-heap
+    for (int b = 0; b < grid; ++b) heap.push_back({0L, b});
+    auto cmp = [](const std::pair<long, int>& a, const std::pair<long, int>& b) { return a > b; };
+    std::make_heap(heap.begin(), heap.end(), cmp);
+    for (int it : order_items) {
+      std::pop_heap(heap.begin(), heap.end(), cmp);
+      auto& top = heap.back();
+      bins[top.second].push_back(it);
+      top.first += cost[it];
+      std::push_heap(heap.begin(), heap.end(), cmp);
+    }
+    int pos = 0;
+    for (int b = 0; b < grid; ++b) {
+      P.begin[b] = (uint16_t)pos;
+      for (int it : bins[b]) P.list[pos++] = (uint16_t)it;
+    }
+    P.begin[grid] = (uint16_t)pos;
+  }
   int max_blocks = 1;
   for (int j = 0; j < count; ++j) max_blocks = std::max(max_blocks, P.prob[j].K / 64);
   P.sc_bytes = S::sc_bytes(max_blocks);
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)std::min(items, num_sms()), 1, 1);
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kPThreads, 1, 1);
   cfg.dynamicSmemBytes = S::total(max_blocks);
   cfg.stream = s;
@@ -462,17 +637,20 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
 }
 
-// decode: 128-element chunks, lane-replicated LUT; GEMM: 64-element chunks, compact LUT
-constexpr int decode_stages(int fmt) { return fmt == WQ_Q8_0 ? 5 : 8; }
+// decode: 256-element chunks, lane-replicated bf16-pair table, block scales folded after the
+// MMA (NVFP4: exact bf16 scaling); GEMM: 64-element chunks, compact fp32 table
+constexpr int decode_stages(int fmt) { return fmt == WQ_Q8_0 ? 3 : 4; }
 constexpr int kGemmStagesP = 4;
 
 template <int FMT>
 int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_static, cudaStream_t s) {
   int64_t maxM = 0;
   for (int i = 0; i < count; ++i) maxM = std::max(maxM, probs[i].M);
-  if (maxM <= 16)
-    return launch_tcp<16, decode_stages(FMT), FMT, 128, 16>(probs, count, out_f32, weights_static, s);
-  return launch_tcp<128, kGemmStagesP, FMT, 64, 1>(probs, count, out_f32, weights_static, s);
+  if (maxM <= 16) {
+    constexpr int mode = FMT == WQ_NVFP4 ? kScaleBF16 : kScaleFold;
+    return launch_tcp<16, decode_stages(FMT), FMT, 256, 32, mode>(probs, count, out_f32, weights_static, s);
+  }
+  return launch_tcp<128, kGemmStagesP, FMT, 64, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
 }
 
 }  // namespace
