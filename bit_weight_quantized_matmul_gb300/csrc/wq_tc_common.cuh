@@ -173,12 +173,12 @@ __device__ __forceinline__ void decode_half(uint32_t sword, const uint8_t* wrow,
 
 // Decode NE (32 or 64) consecutive weights of one 64-element block of a row into NE/2
 // bf16x2 words.  `part` selects which NE-element part of the block (0 when NE == 64);
-// `sword` is the block's scale word (see scale_word); `wsrc` points at the NE packed
-// codes in shared memory.  The byte -> (value, value) table holds LUTREP copies
+// `sword` is the block's scale word (see scale_word); `wv` holds the NE packed codes
+// (16 bytes per entry, already loaded from shared memory).  The byte -> (value, value) table holds LUTREP copies
 // interleaved so that lane group `lsel` reads its own banks (LUTREP = 16: the 16
 // lanes of a half-warp never collide on a 64-bit load, whatever the codes).
 template <int FMT, int NE, int LUTREP>
-__device__ __forceinline__ void decode_span(uint32_t sword, int part, const uint8_t* wsrc, const float2* lut,
+__device__ __forceinline__ void decode_span(uint32_t sword, int part, const uint4* wv, const float2* lut,
                                             int lsel, uint32_t (&out)[NE / 2]) {
   static_assert(NE == 32 || NE == 64, "span");
   if (FMT == WQ_Q8_0) {
@@ -186,7 +186,7 @@ __device__ __forceinline__ void decode_span(uint32_t sword, int part, const uint
     for (int q = 0; q < NE / 16; ++q) {
       const int e0 = part * NE + q * 16;  // element index within the 64-block
       const float d = f16_bits_to_f32(e0 < 32 ? (sword & 0xFFFFu) : (sword >> 16));
-      const uint4 v = reinterpret_cast<const uint4*>(wsrc)[q];
+      const uint4 v = wv[q];
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -200,7 +200,7 @@ __device__ __forceinline__ void decode_span(uint32_t sword, int part, const uint
   }
 #pragma unroll
   for (int q = 0; q < NE / 32; ++q) {
-    const uint4 v = reinterpret_cast<const uint4*>(wsrc)[q];
+    const uint4 v = wv[q];
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -241,13 +241,13 @@ __device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
 // bits).  Unscaled (the per-block scale is applied to the MMA partial sums
 // afterwards): NF4 codebook values in bf16, q4_0 (q - 8), q8_0 q -- the last two exact.
 template <int FMT, int NE, int LUTREP, bool SCALED>
-__device__ __forceinline__ void decode_span_bf16(uint32_t sword, int part, const uint8_t* wsrc,
+__device__ __forceinline__ void decode_span_bf16(uint32_t sword, int part, const uint4* wv,
                                                  const uint32_t* lut, int lsel, uint32_t (&out)[NE / 2]) {
   static_assert(NE == 32 || NE == 64, "span");
   if (FMT == WQ_Q8_0) {
 #pragma unroll
     for (int q = 0; q < NE / 16; ++q) {
-      const uint4 v = reinterpret_cast<const uint4*>(wsrc)[q];
+      const uint4 v = wv[q];
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -259,7 +259,7 @@ __device__ __forceinline__ void decode_span_bf16(uint32_t sword, int part, const
   }
 #pragma unroll
   for (int q = 0; q < NE / 32; ++q) {
-    const uint4 v = reinterpret_cast<const uint4*>(wsrc)[q];
+    const uint4 v = wv[q];
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -278,5 +278,28 @@ __device__ __forceinline__ void decode_span_bf16(uint32_t sword, int part, const
   }
 }
 
+}  // namespace tc
+}  // namespace wq
+
+namespace wq {
+namespace tc {
+// 16-byte chunk `ck` of weight row `r` in a pipeline stage made of NBOX TMA boxes
+// [128 rows x RB bytes], each written with the TMA swizzle of width RB (32/64/128 B:
+// address bits [4, 4+log2(RB/16)) XOR bits [7, ...)), which keeps the 32 rows a warp
+// reads on distinct banks.
+template <int RB, int NBOX>
+__device__ __forceinline__ uint4 load_wchunk(const uint8_t* stage, int r, int ck) {
+  constexpr int CPB = RB / 16;  // chunks per box row
+  constexpr uint32_t mask = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
+  const int box = (NBOX > 1) ? ck / CPB : 0;
+  uint32_t off = (uint32_t)(r * RB + (ck % CPB) * 16);
+  off ^= ((off >> 7) & mask) << 4;
+  return *reinterpret_cast<const uint4*>(stage + box * (128 * RB) + off);
+}
+
+template <int RB>
+constexpr CUtensorMapSwizzle swizzle_of() {
+  return RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : RB == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+}
 }  // namespace tc
 }  // namespace wq

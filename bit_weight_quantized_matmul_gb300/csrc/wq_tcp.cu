@@ -42,7 +42,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kMaxItems = 4096;   // items a launch can schedule with an explicit per-CTA list
+constexpr int kMaxItems = 2560;   // items a launch can schedule with an explicit per-CTA list
 constexpr int kDeqWarps = 8;      // two per TMEM lane quarter, each decoding half of a chunk
 constexpr int kEpiWarp0 = 2 + kDeqWarps;
 constexpr int kScaleWarp = kEpiWarp0 + 4;
@@ -67,7 +67,11 @@ struct PParams {
   int use_list;    // 1: CTA b runs items list[begin[b] .. begin[b+1]); 0: items b, b + grid, ...
   PProblem prob[kGroupMax];
   uint16_t begin[kMaxCtas + 1];
-  uint16_t list[kMaxItems];
+  uint32_t list[kMaxItems];  // packed item coordinates: problem | n-tile << 6 | m-tile << 19
+};
+
+struct ItemCoord {
+  int p, nt, mt;
 };
 
 // The items a CTA runs, in order.
@@ -80,8 +84,8 @@ struct ItemIter {
     else { pos = blockIdx.x; end = P.total_items; step = gridDim.x; }
   }
   __device__ bool more() const { return pos < end; }
-  __device__ int item(const PParams& P) const { return list ? (int)P.list[pos] : pos; }
   __device__ void next() { pos += step; }
+  __device__ ItemCoord coord(const PParams& P) const;
 };
 
 struct PMaps {
@@ -141,16 +145,20 @@ struct PTmem {
   static_assert(USED <= 512, "TMEM budget");
 };
 
-struct ItemCoord {
-  int p, nt, mt;
-};
-
 __device__ __forceinline__ ItemCoord item_coord(const PParams& P, int i) {
   int p = 0;
   while (p + 1 < P.nprob && P.prob[p + 1].item_begin <= i) ++p;
   const int local = i - P.prob[p].item_begin;
   const int nt_count = P.prob[p].ntiles;
   return ItemCoord{p, local % nt_count, local / nt_count};
+}
+
+__device__ __forceinline__ ItemCoord ItemIter::coord(const PParams& P) const {
+  if (list) {
+    const uint32_t v = P.list[pos];
+    return ItemCoord{(int)(v & 63u), (int)((v >> 6) & 8191u), (int)(v >> 19)};
+  }
+  return item_coord(P, pos);
 }
 
 template <int BN, int STAGES, int FMT, int KC, int LUTREP, int MODE>
@@ -162,12 +170,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
   static_assert(MODE != kScaleBF16 || FMT == WQ_NVFP4, "bf16 scaling is exact for NVFP4 only");
   constexpr bool FOLD = MODE == kScaleFold;
   constexpr int kNA = T::NA;
+  // fold warps read chunk g's partials once A slot g % NA is released, and the partial
+  // ring is indexed g & 1: the two rings must coincide
+  static_assert(!FOLD || T::NA == 2, "fold mode pairs the partial ring with the A ring");
   constexpr int SCALE_CONSUMERS = FOLD ? 4 : kDeqWarps;
   constexpr int SUB = S::SUB;
   constexpr int NE = KC / 2;  // elements of a row each dequant warp decodes per chunk
   constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
   constexpr uint32_t STAGE_TX = (uint32_t)(S::XB + S::WB);
   constexpr int WCHUNK = Fmt<FMT>::WB * SUB;  // packed bytes of one row per chunk
+  constexpr int WRB = WCHUNK < 128 ? WCHUNK : 128;  // row bytes of one W TMA box (swizzle width)
+  constexpr int WNBOX = WCHUNK / WRB;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -230,11 +243,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (P.weights_static) {
         int g = 0;
         for (ItemIter ii(P); ii.more() && g < STAGES; ii.next()) {
-          const ItemCoord ic = item_coord(P, ii.item(P));
+          const ItemCoord ic = ii.coord(P);
           const int nch = (P.prob[ic.p].K + KC - 1) / KC;
           for (int c = 0; c < nch && g < STAGES; ++c, ++g) {
             mbar_arrive_expect_tx(&full[g], STAGE_TX);
-            tma_load_2d(smem + S::W_OFF + g * S::WB, &maps.w[ic.p], &full[g], c * WCHUNK, ic.nt * kRows);
+            for (int b = 0; b < WNBOX; ++b)
+              tma_load_2d(smem + S::W_OFF + g * S::WB + b * 128 * WRB, &maps.w[ic.p], &full[g],
+                          c * WCHUNK + b * WRB, ic.nt * kRows);
           }
         }
         pre = g;
@@ -243,14 +258,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int g = 0;
       bool ok = true;
       for (ItemIter ii(P); ii.more() && ok; ii.next()) {
-        const ItemCoord ic = item_coord(P, ii.item(P));
+        const ItemCoord ic = ii.coord(P);
         const int nch = (P.prob[ic.p].K + KC - 1) / KC;
         for (int c = 0; c < nch; ++c, ++g) {
           const int s = g % STAGES;
           if (g >= pre) {
+            // stage s is free once chunk g - STAGES is consumed (x by its MMAs, weights by the
+            // dequant warps); a per-stage barrier cannot complete twice before this wait
             if (g >= STAGES && !mbar_wait(&empty[s], ((g / STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(&full[s], STAGE_TX);
-            tma_load_2d(smem + S::W_OFF + s * S::WB, &maps.w[ic.p], &full[s], c * WCHUNK, ic.nt * kRows);
+            for (int b = 0; b < WNBOX; ++b)
+              tma_load_2d(smem + S::W_OFF + s * S::WB + b * 128 * WRB, &maps.w[ic.p], &full[s],
+                          c * WCHUNK + b * WRB, ic.nt * kRows);
           }
 #pragma unroll
           for (int j = 0; j < SUB; ++j)
@@ -267,7 +286,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int g = 0, n_it = 0;
       bool ok = true;
       for (ItemIter ii(P); ii.more() && ok; ii.next(), ++n_it) {
-        const ItemCoord ic = item_coord(P, ii.item(P));
+        const ItemCoord ic = ii.coord(P);
         const int nch = (P.prob[ic.p].K + KC - 1) / KC;
         const int buf = n_it & 1;
         if (!FOLD && !mbar_wait_lanes(&dempty[buf], ((n_it >> 1) & 1) ^ 1, lane == 0 && n_it >= 2, abort_flag))
@@ -285,20 +304,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (lane == 0) {
             const uint32_t xaddr = smem_u32(smem + S::X_OFF + s * S::XB);
 #pragma unroll
-            for (int kk = 0; kk < KC / 16; ++kk) {
-              const uint64_t bdesc = smem_desc(xaddr + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024, 2);
-              const uint32_t a_tmem = tmem_base + slot * T::ACOLS + kk * 8;
+            for (int i = 0; i < KC / 16; ++i) {
               if (FOLD) {
+                // consecutive MMAs go to different scale blocks' partial tiles
                 constexpr int KPG = (KC / 16) / T::G;  // MMA K steps per scale block
-                const uint32_t p_tmem = tmem_base + T::D_COL + ((g & 1) * T::G + kk / KPG) * BN;
-                mma_bf16_ts(p_tmem, a_tmem, bdesc, IDESC, (kk % KPG) != 0 ? 1u : 0u);
+                const int grp = i % T::G, step = i / T::G, kk = grp * KPG + step;
+                const uint64_t bdesc = smem_desc(xaddr + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024, 2);
+                const uint32_t p_tmem = tmem_base + T::D_COL + ((g & 1) * T::G + grp) * BN;
+                mma_bf16_ts(p_tmem, tmem_base + slot * T::ACOLS + kk * 8, bdesc, IDESC, step != 0 ? 1u : 0u);
               } else {
-                mma_bf16_ts(d_tmem, a_tmem, bdesc, IDESC, (c | kk) != 0 ? 1u : 0u);
+                const int kk = i;
+                const uint64_t bdesc = smem_desc(xaddr + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024, 2);
+                mma_bf16_ts(d_tmem, tmem_base + slot * T::ACOLS + kk * 8, bdesc, IDESC, (c | kk) != 0 ? 1u : 0u);
               }
             }
             tc_commit(&aempty[slot]);
             tc_commit(&empty[s]);
-            if (FOLD) tc_commit(&dfull[g & 1]);
           }
           __syncwarp();
         }
@@ -316,7 +337,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     int g = 0, n_it = 0;
     bool ok = true;
     for (ItemIter ii(P); ii.more() && ok; ii.next(), ++n_it) {
-      const ItemCoord ic = item_coord(P, ii.item(P));
+      const ItemCoord ic = ii.coord(P);
       const PProblem& pr = P.prob[ic.p];
       const int nb = pr.K / 64;                 // 64-element blocks per row
       const int nch = (pr.K + KC - 1) / KC;
@@ -349,17 +370,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         if (!mbar_wait(&full[s], (g / STAGES) & 1, abort_flag)) { ok = false; break; }
         if (g >= kNA && !mbar_wait(&aempty[slot], ((g / kNA) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        const uint8_t* wsrc = smem + S::W_OFF + s * S::WB + r * WCHUNK + h * (WCHUNK / 2);
-        constexpr int NES = NE / NBW;  // elements per decode call (32 or 64)
+        const uint8_t* wstage = smem + S::W_OFF + s * S::WB;
+        constexpr int NES = NE / NBW;                          // elements per decode call (32 or 64)
+        constexpr int CPS = NES / (FMT == WQ_Q8_0 ? 16 : 32);  // 16-byte chunks per call
+        const int ck0 = h * (WCHUNK / 32);                      // first chunk of this warp's half row
 #pragma unroll
         for (int bb = 0; bb < NBW; ++bb) {
           uint32_t v[NES / 2];
+          uint4 wv[CPS];
+#pragma unroll
+          for (int k = 0; k < CPS; ++k) wv[k] = load_wchunk<WRB, WNBOX>(wstage, r, ck0 + bb * CPS + k);
           const int part = (KC == 64) ? h : 0;
-          const uint8_t* src = wsrc + bb * (WCHUNK / (2 * NBW));
           if (MODE == kScaleF32)
-            decode_span<FMT, NES, LUTREP>(sword[bb], part, src, lut, lsel, v);
+            decode_span<FMT, NES, LUTREP>(sword[bb], part, wv, lut, lsel, v);
           else
-            decode_span_bf16<FMT, NES, LUTREP, MODE == kScaleBF16>(sword[bb], part, src, lut32, lsel, v);
+            decode_span_bf16<FMT, NES, LUTREP, MODE == kScaleBF16>(sword[bb], part, wv, lut32, lsel, v);
           tmem_st_n(tmem_base + lane_base + slot * T::ACOLS + h * (NE / 2) + bb * (NES / 2), v);
         }
         tc_wait_st();
@@ -378,7 +403,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     griddep_wait();
     int n_it = 0, g = 0;
     for (ItemIter ii(P); ii.more(); ii.next(), ++n_it) {
-      const ItemCoord ic = item_coord(P, ii.item(P));
+      const ItemCoord ic = ii.coord(P);
       const PProblem& pr = P.prob[ic.p];
       const int buf = n_it & 1;
       const int64_t n = (int64_t)ic.nt * kRows + r;
@@ -419,7 +444,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             sg[grp] = sv;
           }
-          if (!mbar_wait(&dfull[g & 1], (g >> 1) & 1, abort_flag)) { ok = false; break; }
+          // the partials of chunk g are complete when its MMAs release A slot g % NA (== g & 1)
+          if (!mbar_wait(&aempty[g % kNA], (g / kNA) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int grp = 0; grp < T::G; ++grp) {
@@ -481,7 +507,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // one bulk copy of the tile's scale slice (contiguous in the blob) into shared memory
     int n_it = 0;
     for (ItemIter ii(P); ii.more(); ii.next(), ++n_it) {
-      const ItemCoord ic = item_coord(P, ii.item(P));
+      const ItemCoord ic = ii.coord(P);
       const PProblem& pr = P.prob[ic.p];
       const int nb = pr.K / 64;
       const int sb = n_it & 1;
@@ -578,7 +604,8 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
                         (uint64_t)a.K * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
       return WQ_ERR_CUDA;
     if (!encode_tmap_2d(&maps.w[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, wrow, (uint64_t)a.N, wrow,
-                        Fmt<FMT>::WB * (KC / 64), kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                        std::min(Fmt<FMT>::WB * (KC / 64), 128), kRows,
+                        swizzle_of<std::min(Fmt<FMT>::WB * (KC / 64), 128)>()))
       return WQ_ERR_CUDA;
   }
   P.total_items = items;
@@ -586,7 +613,10 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   const int grid = std::min(std::min(items, num_sms()), kMaxCtas);
   // longest-processing-time-first assignment of items to CTAs (cost = K chunks + a fixed
   // per-item overhead); items are visited heaviest first, each to the least-loaded CTA
-  P.use_list = items <= kMaxItems ? 1 : 0;
+  P.use_list = 1;
+  if (items > kMaxItems) P.use_list = 0;
+  for (int j = 0; j < count; ++j)
+    if (P.prob[j].ntiles > 8191 || P.prob[j].mtiles > 8191) P.use_list = 0;
   if (P.use_list) {
     std::vector<int> order_items(items);
     std::vector<int> cost(items);
@@ -607,10 +637,15 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
       top.first += cost[it];
       std::push_heap(heap.begin(), heap.end(), cmp);
     }
+    std::vector<uint32_t> packed(items);
+    for (int j = 0; j < count; ++j)
+      for (int i = 0; i < P.prob[j].ntiles * P.prob[j].mtiles; ++i)
+        packed[P.prob[j].item_begin + i] =
+            (uint32_t)j | ((uint32_t)(i % P.prob[j].ntiles) << 6) | ((uint32_t)(i / P.prob[j].ntiles) << 19);
     int pos = 0;
     for (int b = 0; b < grid; ++b) {
       P.begin[b] = (uint16_t)pos;
-      for (int it : bins[b]) P.list[pos++] = (uint16_t)it;
+      for (int it : bins[b]) P.list[pos++] = packed[it];
     }
     P.begin[grid] = (uint16_t)pos;
   }
