@@ -129,3 +129,26 @@ def test_m_zero_is_noop():
     y = torch.zeros((0, 128), dtype=torch.bfloat16, device="cuda")
     wq().linear_into(y, x, packed, scales, "nf4", 128, 128)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M,K", [(128, 256), (300, 512)])
+def test_w4a4_tensor_path_is_exact_products(M, K):
+    """W4A4 on the block-scaled FP4 tensor cores: every product e2m1 * e4m3 * e2m1 * e4m3 is exact
+    in fp32, so the fp32 output differs from the fp64 oracle only by the accumulation order and the
+    two epilogue roundings: |err| <= (K * 2^-24 + 2^-22) * sum |x_hat| |w_hat|."""
+    need_gpu()
+    N = 256
+    W = weight_np(77 + K, N, K)
+    x = wl.activations(77 + M, M, K, outlier_frac=0.001)
+    p_ref = oracle_pack("nvfp4", W)
+    xf = wl.bf16_as_f32(x)
+    a = Q.quant_act_nvfp4(xf)
+    x_hat = Q.nvfp4_dequant_parts(a["codes"], a["scales"], a["g"]).astype(np.float64)
+    w_hat = Q.nvfp4_dequant(p_ref).astype(np.float64)
+    y_ref = x_hat @ w_hat.T
+    packed, scales = gpu_pack("nvfp4", W)
+    y = wq().linear(wq().quant_act_nvfp4(x.cuda()), packed, scales, "nvfp4_w4a4", N, K, out_f32=True)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    bound = (K * 2.0 ** -24 + 2.0 ** -22) * (np.abs(x_hat) @ np.abs(w_hat).T) + 1e-30
+    assert np.all(np.abs(got - y_ref) <= bound), float(np.max(np.abs(got - y_ref) / bound))
