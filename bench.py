@@ -40,6 +40,22 @@ def dist_env():
         int(os.environ.get("WORLD_SIZE", "1"))
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step, steps, world, t_seconds_max):
+    """Whole-job GB/s: every rank processed its own copy of the workload (weak scaling)."""
+    return world * bytes_per_rank_step * steps / t_seconds_max / 1e9
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if not os.path.exists(path):
@@ -209,12 +225,7 @@ def run_ours(args, rank, local_rank, world):
             ev1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        t = ev0.elapsed_time(ev1)
-        if world > 1:
-            tt = torch.tensor([t], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t = float(tt.item())
-        return t
+        return max_over_ranks(ev0.elapsed_time(ev1), world, dev)
 
     with torch.cuda.stream(stream):
         for w in range(args.warmup):
@@ -227,7 +238,7 @@ def run_ours(args, rank, local_rank, world):
     t_ms = timed(graphs, args.steps)
     clk = clocks.stop()
     ms_per_step = t_ms / args.steps
-    value = world * bytes_per_step * args.steps / (t_ms * 1e-3) / 1e9  # GB/s, all ranks
+    value = job_throughput(bytes_per_step, args.steps, world, t_ms * 1e-3)  # GB/s, all ranks
     ch_steps = max(3, min(args.steps, 2000))
     t_ch = timed(chained_graphs, ch_steps)
     chained = {"value": round(bytes_per_step * ch_steps / (t_ch * 1e-3) / 1e9, 2), "unit": "GB/s",
@@ -259,12 +270,8 @@ def run_ours(args, rank, local_rank, world):
     t0 = time.perf_counter()
     for k in range(e2e_steps):
         e2e_step(k)
-    t_e2e = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = float(t.item())
-    e2e_value = world * bytes_per_step * e2e_steps / t_e2e / 1e9
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e_value = job_throughput(bytes_per_step, e2e_steps, world, t_e2e)
 
     peaks = read_peaks()
     pk, pk_src = peak_hbm(peaks)
@@ -313,31 +320,49 @@ def load_traffic(kernel, workload):
 
 
 def extra_gemm(wq, wl, dev, peaks):
-    """Encoder-side context: NVFP4 W4A16 fc1 GEMM at M = 1500 x 4 (TFLOPS, L2-cold weights)."""
+    """Encoder-side context (configs 2 and 3 shapes): the fc1 Linear (N=5120, K=1280) at
+    M = 1500 x 4 in NVFP4 W4A16, and in W4A4 (GEMM alone, and with the runtime activation
+    quantiser); L2 flushed before every launch; median of 10."""
     import torch
     M, N, K = 6000, 5120, 1280
     W = torch.from_numpy(wl.weight(101, N, K)).to(dev)
     p, s = wq.pack("nvfp4", W)
     x = wl.activations(101, M, K, outlier_frac=0.001).to(dev)
+    b = wl.bias(101, N).to(dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    act = (torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+           torch.empty((M, K // 16), dtype=torch.uint8, device=dev),
+           torch.empty(1, dtype=torch.float32, device=dev))
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    for _ in range(3):
-        wq.linear_into(y, x, p, s, "nvfp4", N, K)
-    times = []
-    for _ in range(10):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        wq.linear_into(y, x, p, s, "nvfp4", N, K)
-        e1.record()
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
-    t = statistics.median(times)
-    tflops = 2.0 * M * N * K / (t * 1e-3) / 1e12
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(10):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    t16 = timed(lambda: wq.linear_into(y, x, p, s, "nvfp4", N, K, b))
+    wq.quant_act_nvfp4(x, out=act)
+    t44 = timed(lambda: wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b))
+    t44q = timed(lambda: (wq.quant_act_nvfp4(x, out=act), wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b)))
+    fl = 2.0 * M * N * K
     pk, src = peak_tflops(peaks, sustained=False)
-    return {"workload": "encoder fc1 NVFP4 W4A16, M=6000 N=5120 K=1280 (B=4 windows)",
-            "value": round(tflops, 1), "unit": "TFLOP/s", "ms": round(t, 4),
-            "roofline": {"bound": "tensor", "peak": pk, "peak_source": src, "frac": round(tflops / pk, 4)}}
+    tf = lambda t: round(fl / (t * 1e-3) / 1e12, 1)
+    return {"workload": "encoder fc1 (N=5120, K=1280) at M=6000 (4 x 1500 frames), L2 flushed",
+            "w4a16_nvfp4": {"value": tf(t16), "unit": "TFLOP/s", "ms": round(t16, 4),
+                            "frac_of_bf16_peak": round(tf(t16) / pk, 4)},
+            "w4a4_nvfp4_gemm": {"value": tf(t44), "unit": "TFLOP/s", "ms": round(t44, 4),
+                                "frac_of_fp4_nominal": round(tf(t44) / (4 * pk), 4)},
+            "w4a4_nvfp4_with_act_quant": {"value": tf(t44q), "unit": "TFLOP/s", "ms": round(t44q, 4)},
+            "peak": {"bf16": pk, "source": src, "fp4": "4 x bf16 (nominal ratio)"}}
 
 
 # ---------------------------------------------------------------- CPU oracle

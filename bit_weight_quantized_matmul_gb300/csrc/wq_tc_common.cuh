@@ -303,3 +303,51 @@ constexpr CUtensorMapSwizzle swizzle_of() {
 }
 }  // namespace tc
 }  // namespace wq
+
+namespace wq {
+namespace tc {
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Eight E2M1 codes (nibbles of u, element 2j in the low nibble of byte j) -> four packed bf16
+// pairs, without tables in memory.  The 3-bit magnitude of a code indexes the 8 bytes of two
+// registers in one byte permute: the high and the low bytes of the bf16 values of
+// {0, .5, 1, 1.5, 2, 3, 4, 6} are 00 3F 3F 3F 40 40 40 40 and 00 00 80 C0 00 40 80 C0.  The sign
+// bit of each code is replicated into bit 15 / 31 with prmt's sign-replicating selectors.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t u, uint32_t (&w)[4]) {
+  constexpr uint32_t H0 = 0x3F3F3F00u, H1 = 0x40404040u, L0 = 0xC0800000u, L1 = 0xC0804000u;
+  const uint32_t sa = u & 0x7777u, sb = (u >> 16) & 0x7777u;
+  const uint32_t hiA = prmt(H0, H1, sa), loA = prmt(L0, L1, sa);
+  const uint32_t hiB = prmt(H0, H1, sb), loB = prmt(L0, L1, sb);
+  const uint32_t u4 = u << 4;  // moves each low nibble's sign bit to its byte's msb
+  w[0] = prmt(loA, hiA, 0x5140u) | (prmt(u, u4, 0x80C0u) & 0x80008000u);
+  w[1] = prmt(loA, hiA, 0x7362u) | (prmt(u, u4, 0x90D0u) & 0x80008000u);
+  w[2] = prmt(loB, hiB, 0x5140u) | (prmt(u, u4, 0xA0E0u) & 0x80008000u);
+  w[3] = prmt(loB, hiB, 0x7362u) | (prmt(u, u4, 0xB0F0u) & 0x80008000u);
+}
+
+// NVFP4: decode NE elements of one 64-element block with E2M1 -> bf16 in registers and the
+// block's E4M3 scales applied as an exact bf16 product.
+template <int NE>
+__device__ __forceinline__ void decode_span_nvfp4_reg(uint32_t sword, int part, const uint4* wv,
+                                                      uint32_t (&out)[NE / 2]) {
+#pragma unroll
+  for (int q = 0; q < NE / 32; ++q) {
+    const uint32_t u[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e0 = part * NE + q * 32 + j * 8;
+      const uint32_t sb = __float_as_uint(e4m3_to_f32((sword >> (8 * (e0 / 16))) & 0xFFu)) >> 16;
+      const uint32_t spair = sb | (sb << 16);
+      uint32_t w[4];
+      e2m1x8_to_bf16(u[j], w);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) out[q * 16 + j * 4 + b] = hmul2_bf16(w[b], spair);
+    }
+  }
+}
+}  // namespace tc
+}  // namespace wq

@@ -43,7 +43,8 @@ namespace {
 using namespace tc;
 
 constexpr int kMaxItems = 2560;   // items a launch can schedule with an explicit per-CTA list
-constexpr int kDeqWarps = 8;      // two per TMEM lane quarter, each decoding half of a chunk
+constexpr int kDeqQ = 2;          // dequant warps per TMEM lane quarter, each decoding 1/kDeqQ of a chunk
+constexpr int kDeqWarps = 4 * kDeqQ;
 constexpr int kEpiWarp0 = 2 + kDeqWarps;
 constexpr int kScaleWarp = kEpiWarp0 + 4;
 constexpr int kPThreads = (kScaleWarp + 1) * 32;  // 15 warps
@@ -116,7 +117,7 @@ struct PSmem {
   static constexpr int X_OFF = 0;
   static constexpr int W_OFF = X_OFF + STAGES * XB;
   static constexpr int LUT_OFF = W_OFF + STAGES * WB;
-  static constexpr int LUT_BYTES = (FMT == WQ_Q8_0) ? 0 : 256 * (MODE == kScaleF32 ? 8 : 4) * LUTREP;
+  static constexpr int LUT_BYTES = (FMT == WQ_Q8_0 || LUTREP == 0) ? 0 : 256 * (MODE == kScaleF32 ? 8 : 4) * LUTREP;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
   static constexpr int NBAR = 2 * STAGES + 2 * a_slots<KC>() + 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   using T = PTmem<BN, KC, FMT, MODE>;
   static_assert(MODE != kScaleFold || (BN == 16 && FMT != WQ_NVFP4), "fold mode: decode tiles");
   static_assert(MODE != kScaleBF16 || FMT == WQ_NVFP4, "bf16 scaling is exact for NVFP4 only");
+  static_assert(LUTREP != 0 || (FMT == WQ_NVFP4 && MODE == kScaleBF16), "register decode: NVFP4");
   constexpr bool FOLD = MODE == kScaleFold;
   constexpr int kNA = T::NA;
   // fold warps read chunk g's partials once A slot g % NA is released, and the partial
@@ -175,7 +177,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   static_assert(!FOLD || T::NA == 2, "fold mode pairs the partial ring with the A ring");
   constexpr int SCALE_CONSUMERS = FOLD ? 4 : kDeqWarps;
   constexpr int SUB = S::SUB;
-  constexpr int NE = KC / 2;  // elements of a row each dequant warp decodes per chunk
+  constexpr int NE = KC / kDeqQ;  // elements of a row each dequant warp decodes per chunk
+  static_assert(NE == 32 || NE % 64 == 0, "a dequant warp decodes half a 64-block or whole blocks");
   constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
   constexpr uint32_t STAGE_TX = (uint32_t)(S::XB + S::WB);
   constexpr int WCHUNK = Fmt<FMT>::WB * SUB;  // packed bytes of one row per chunk
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (FMT != WQ_Q8_0) {
+  if (FMT != WQ_Q8_0 && LUTREP > 0) {
     for (int i = threadIdx.x; i < 256 * LUTREP; i += kPThreads) {
       const uint32_t b = (uint32_t)(i / LUTREP);
       if (MODE == kScaleF32)
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------ dequant warps: half h of every chunk
     const int q = warp & 3;
-    const int h = (warp - 2) / 4;
+    const int h = (warp - 2) / 4;  // which 1/kDeqQ of the chunk
     const int r = q * 32 + lane;
     const int lsel = (LUTREP > 1) ? (lane & (LUTREP - 1)) : 0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -351,12 +354,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const float off = (FMT == WQ_NF4 && !FOLD) ? s2s[kS2Max - 1] : 0.0f;
       for (int c = 0; c < nch; ++c, ++g) {
         const int s = g % STAGES, slot = g % kNA;
-        constexpr int NBW = (KC >= 128) ? NE / 64 : 1;  // 64-blocks this warp decodes per chunk
+        constexpr int NBW = (NE >= 64) ? NE / 64 : 1;  // 64-blocks (or half of one) this warp decodes
         uint32_t sword[NBW];
 #pragma unroll
         for (int bb = 0; bb < NBW; ++bb) {
-          // the 64-block this warp decodes (KC >= 128), or the block holding its half (KC == 64)
-          const int blk = (KC >= 128) ? (KC / 64) * c + NBW * h + bb : c;
+          // the 64-block this warp decodes (NE >= 64), or the block holding its half (NE == 32)
+          const int blk = (NE >= 64) ? (KC / 64) * c + NBW * h + bb : (KC / 64) * c + h / 2;
           sword[bb] = 0u;
           if (!FOLD && row_ok && blk < nb) {
             if (FMT == WQ_NF4) {
@@ -373,15 +376,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint8_t* wstage = smem + S::W_OFF + s * S::WB;
         constexpr int NES = NE / NBW;                          // elements per decode call (32 or 64)
         constexpr int CPS = NES / (FMT == WQ_Q8_0 ? 16 : 32);  // 16-byte chunks per call
-        const int ck0 = h * (WCHUNK / 32);                      // first chunk of this warp's half row
+        const int ck0 = h * (WCHUNK / (16 * kDeqQ));            // first 16-byte chunk of this warp's part
 #pragma unroll
         for (int bb = 0; bb < NBW; ++bb) {
           uint32_t v[NES / 2];
           uint4 wv[CPS];
 #pragma unroll
           for (int k = 0; k < CPS; ++k) wv[k] = load_wchunk<WRB, WNBOX>(wstage, r, ck0 + bb * CPS + k);
-          const int part = (KC == 64) ? h : 0;
-          if (MODE == kScaleF32)
+          const int part = (NE == 32) ? (h & 1) : 0;
+          if constexpr (LUTREP == 0)
+            decode_span_nvfp4_reg<NES>(sword[bb], part, wv, v);
+          else if constexpr (MODE == kScaleF32)
             decode_span<FMT, NES, LUTREP>(sword[bb], part, wv, lut, lsel, v);
           else
             decode_span_bf16<FMT, NES, LUTREP, MODE == kScaleBF16>(sword[bb], part, wv, lut32, lsel, v);
@@ -673,19 +678,23 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
 }
 
 // decode: 256-element chunks, lane-replicated bf16-pair table, block scales folded after the
-// MMA (NVFP4: exact bf16 scaling); GEMM: 64-element chunks, compact fp32 table
+// MMA (NVFP4: exact bf16 scaling); GEMM: 128-element chunks, compact fp32 table
 constexpr int decode_stages(int fmt) { return fmt == WQ_Q8_0 ? 3 : 4; }
-constexpr int kGemmStagesP = 4;
+constexpr int kGemmStagesP = 3;
 
 template <int FMT>
 int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_static, cudaStream_t s) {
   int64_t maxM = 0;
   for (int i = 0; i < count; ++i) maxM = std::max(maxM, probs[i].M);
+  // NVFP4 decodes E2M1 in registers (no table) and scales exactly in bf16
   if (maxM <= 16) {
     constexpr int mode = FMT == WQ_NVFP4 ? kScaleBF16 : kScaleFold;
-    return launch_tcp<16, decode_stages(FMT), FMT, 256, 32, mode>(probs, count, out_f32, weights_static, s);
+    constexpr int rep = FMT == WQ_NVFP4 ? 0 : 32;
+    return launch_tcp<16, decode_stages(FMT), FMT, 256, rep, mode>(probs, count, out_f32, weights_static, s);
   }
-  return launch_tcp<128, kGemmStagesP, FMT, 64, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
+  if constexpr (FMT == WQ_NVFP4)
+    return launch_tcp<128, kGemmStagesP, FMT, 128, 0, kScaleBF16>(probs, count, out_f32, weights_static, s);
+  return launch_tcp<128, kGemmStagesP, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
 }
 
 }  // namespace
