@@ -141,7 +141,9 @@ struct PTmem {
   static constexpr int D_COL = NA * ACOLS;
   // kScaleFold: a double-buffered ring of per-scale-block partial tiles instead of D
   static constexpr int G = scale_groups_per_128<FMT>() * KC / 128;
-  static constexpr int USED = D_COL + 2 * BN * (MODE == kScaleFold ? G : 1);
+  // accumulator buffers: two (epilogue overlaps the next item) when they fit next to the A ring
+  static constexpr int NDB = (MODE == kScaleFold || D_COL + 2 * BN <= 512) ? 2 : 1;
+  static constexpr int USED = D_COL + NDB * BN * (MODE == kScaleFold ? G : 1);
   static constexpr int ALLOC = USED <= 256 ? 256 : 512;
   static_assert(USED <= 512, "TMEM budget");
 };
@@ -291,8 +293,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (ItemIter ii(P); ii.more() && ok; ii.next(), ++n_it) {
         const ItemCoord ic = ii.coord(P);
         const int nch = (P.prob[ic.p].K + KC - 1) / KC;
-        const int buf = n_it & 1;
-        if (!FOLD && !mbar_wait_lanes(&dempty[buf], ((n_it >> 1) & 1) ^ 1, lane == 0 && n_it >= 2, abort_flag))
+        const int buf = n_it % T::NDB;
+        if (!FOLD && !mbar_wait_lanes(&dempty[buf], ((n_it / T::NDB) & 1) ^ 1, lane == 0 && n_it >= T::NDB,
+                                      abort_flag))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + T::D_COL + buf * BN;
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (ItemIter ii(P); ii.more(); ii.next(), ++n_it) {
       const ItemCoord ic = ii.coord(P);
       const PProblem& pr = P.prob[ic.p];
-      const int buf = n_it & 1;
+      const int buf = n_it % T::NDB;
       const int64_t n = (int64_t)ic.nt * kRows + r;
       const bool row_ok = n < pr.N;
       const float gsc = (FMT == WQ_NVFP4) ? *reinterpret_cast<const float*>(pr.scales + pr.lay.g_off) : 1.0f;
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         continue;
       }
-      if (!mbar_wait(&dfull[buf], (n_it >> 1) & 1, abort_flag)) break;
+      if (!mbar_wait(&dfull[buf], (n_it / T::NDB) & 1, abort_flag)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -692,8 +695,12 @@ int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_st
     constexpr int rep = FMT == WQ_NVFP4 ? 0 : 32;
     return launch_tcp<16, decode_stages(FMT), FMT, 256, rep, mode>(probs, count, out_f32, weights_static, s);
   }
+  // GEMM: 256 activation rows per tile (N = 256 MMAs, one TMEM accumulator) where shared memory
+  // allows two stages of them; 128 rows (two accumulators) for q4_0 / q8_0
   if constexpr (FMT == WQ_NVFP4)
-    return launch_tcp<128, kGemmStagesP, FMT, 128, 0, kScaleBF16>(probs, count, out_f32, weights_static, s);
+    return launch_tcp<256, 2, FMT, 128, 0, kScaleBF16>(probs, count, out_f32, weights_static, s);
+  if constexpr (FMT == WQ_NF4)
+    return launch_tcp<256, 2, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
   return launch_tcp<128, kGemmStagesP, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
 }
 
