@@ -378,6 +378,83 @@ def extra_gemm(wq, wl, dev, peaks):
             "peak": {"bf16": pk, "source": src, "fp4": "4 x bf16 (nominal ratio)"}}
 
 
+# ---------------------------------------------------------------- encoder workloads
+def run_encoder(args, rank, local_rank, world):
+    """Configs 2 / 3: the encoder Linear shapes (q/k/v/o 1280x1280, fc1 5120x1280, fc2
+    1280x5120) at M = 1500 x B for B in {1, 4, 16}, NVFP4 weights, bf16 activations with 0.1 %
+    outliers x20; W4A16, or W4A4 with the runtime activation quantiser inside the step.  One step
+    = the 9 GEMMs; each launch is timed with CUDA events after an L2 flush (excluded)."""
+    import torch
+    from bit_weight_quantized_matmul_gb300 import build as B
+    B.build()
+    from bit_weight_quantized_matmul_gb300 import wq
+    from bit_weight_quantized_matmul_gb300 import workloads as wl
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w4a4 = args.workload == "encoder_w4a4"
+    cases = []
+    for si, (name, N, K) in enumerate(wl.encoder_shapes()):
+        W = torch.from_numpy(wl.weight(100 + si, N, K)).to(dev)
+        p, s = wq.pack("nvfp4", W)
+        b = wl.bias(100 + si, N).to(dev)
+        for Bw in (1, 4, 16):
+            M = 1500 * Bw
+            x = wl.activations(100 + si, M, K, outlier_frac=0.001).to(dev)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            act = (torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                   torch.empty((M, K // 16), dtype=torch.uint8, device=dev),
+                   torch.empty(1, dtype=torch.float32, device=dev))
+            cases.append(dict(name=name, B=Bw, M=M, N=N, K=K, p=p, s=s, b=b, x=x, y=y, act=act))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def launch(c):
+        if w4a4:
+            wq.quant_act_nvfp4(c["x"], out=c["act"])
+            wq.linear_into(c["y"], c["act"], c["p"], c["s"], "nvfp4_w4a4", c["N"], c["K"], c["b"])
+        else:
+            wq.linear_into(c["y"], c["x"], c["p"], c["s"], "nvfp4", c["N"], c["K"], c["b"])
+
+    for _ in range(args.warmup):
+        for c in cases:
+            launch(c)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(len(cases) * args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    k = 0
+    for _ in range(args.steps):
+        for c in cases:
+            flush.zero_()
+            ev[k][0].record()
+            launch(c)
+            ev[k][1].record()
+            k += 1
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    per = [e0.elapsed_time(e1) for e0, e1 in ev]
+    t_ms = max_over_ranks(sum(per), world, dev)
+    flops_step = sum(2.0 * c["M"] * c["N"] * c["K"] for c in cases)
+    value = world * flops_step * args.steps / (t_ms * 1e-3) / 1e12
+    peaks = read_peaks()
+    pk, src = peak_tflops(peaks, sustained=False)
+    by = {}
+    for i, c in enumerate(cases):
+        ts = sorted(per[j] for j in range(i, len(per), len(cases)))
+        by[f"{c['name']}_B{c['B']}"] = round(2.0 * c["M"] * c["N"] * c["K"] / (ts[len(ts) // 2] * 1e-3) / 1e12, 1)
+    return {"metric": "4-bit dequant-linear TFLOP/s, encoder (M = 1500 x B)", "value": round(value, 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4 weights, " + ("nvfp4 activations" if w4a4 else "bf16 activations"),
+            "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": ("W4A4 (activation quantiser in the step)" if w4a4 else "W4A16") +
+                                   ": encoder Linears qkvo/fc1/fc2 at M=1500*B, B in {1,4,16} (9 GEMMs/step)",
+                       "l2": "flushed (256 MB write) before every launch, outside the timed events"},
+            "roofline": {"bound": "tensor", "achieved": round(value / world, 2), "peak": pk * (4 if w4a4 else 1),
+                         "unit": "TFLOP/s", "frac": round(value / world / (pk * (4 if w4a4 else 1)), 4),
+                         "peak_source": src + (" bf16 x 4 (nominal fp4 ratio)" if w4a4 else ""), "traffic": None},
+            "per_gemm_tflops_median": by, "clocks": clk, "gpu_launches": len(per) * (3 if w4a4 else 1)}
+
+
 # ---------------------------------------------------------------- CPU oracle
 _ORACLE_CACHE = {}
 
@@ -457,6 +534,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
+    ap.add_argument("--workload", default="decoder_nf4", choices=["decoder_nf4", "encoder_w4a16", "encoder_w4a4"])
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, local_rank, world = dist_env()
@@ -468,7 +546,8 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    out = run_ours(args, rank, local_rank, world)
+    out = run_ours(args, rank, local_rank, world) if args.workload == "decoder_nf4" else \
+        run_encoder(args, rank, local_rank, world)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -351,3 +351,40 @@ __device__ __forceinline__ void decode_span_nvfp4_reg(uint32_t sword, int part, 
 }
 }  // namespace tc
 }  // namespace wq
+
+namespace wq {
+namespace tc {
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Store one 16-column slab of a D tile (TMEM lanes = 128 weight rows n0.., columns = 16
+// activation rows m0..) to y[M, N] bf16 through shared memory: each of the 128 epilogue
+// threads (its TMEM lane r) scales and writes its 16 values into stage[m][r], then the
+// threads copy the [16 x 128] bf16 slab out as whole 256-byte rows with 16-byte stores.
+// `stage` is this slab's 4 KB buffer; callers alternate two buffers (one barrier per slab).
+__device__ __forceinline__ void store_slab_bf16(const float (&acc)[16], float gsc, float bval, int r,
+                                                uint16_t* stage, void* y, int64_t M, int64_t N, int64_t m0,
+                                                int64_t n0) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float v = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
+    stage[j * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  epi_bar();
+  // thread t copies 16 elements: row t / 8, columns (t % 8) * 16 .. + 15
+  const int row = r >> 3, seg = (r & 7) * 16;
+  const int64_t m = m0 + row, n = n0 + seg;
+  if (m < M && n < N) {
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(y) + m * N + n;
+    const uint16_t* src = stage + row * 128 + seg;
+    if (n + 16 <= N && (N & 7) == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      d4[0] = s4[0];
+      d4[1] = s4[1];
+    } else {
+      for (int e = 0; e < 16 && n + e < N; ++e) reinterpret_cast<uint16_t*>(dst)[e] = src[e];
+    }
+  }
+}
+}  // namespace tc
+}  // namespace wq

@@ -121,14 +121,20 @@ struct PSmem {
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
   static constexpr int NBAR = 2 * STAGES + 2 * a_slots<KC>() + 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int S2_OFF = (MISC_OFF + 16 + 15) / 16 * 16;               // [2][kS2Max] NF4 s2 + offset
+  static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;             // [2] 4 KB output slabs
+  static constexpr int S2_OFF = Y_OFF + 2 * 16 * kRows * 2;                   // [2][kS2Max] NF4 s2 + offset
   static constexpr int SC_OFF = (S2_OFF + 2 * kS2Max * 4 + 127) / 128 * 128;  // [2] raw scale slices
   static constexpr int FIXED = SC_OFF + 1024;                                   // + alignment slack
   // one tile's scale bytes as stored in the blob (row-major): 4 bytes per row per
   // 64-block (NVFP4 / q4_0 / q8_0), 1 byte (NF4); two buffers
   static constexpr int sc_bytes(int blocks) { return blocks * kRows * (FMT == WQ_NF4 ? 1 : 4); }
   static constexpr int total(int blocks) { return FIXED + 2 * sc_bytes(blocks); }
-  static_assert(total(kMaxChunks) <= 227 * 1024, "shared memory budget");
+  // the longest K (in 64-blocks) whose scale slices fit next to the pipeline
+  static constexpr int max_blocks() {
+    const int fit = (227 * 1024 - FIXED) / (2 * kRows * (FMT == WQ_NF4 ? 1 : 4));
+    return fit < kMaxChunks ? fit : kMaxChunks;
+  }
+  static_assert(max_blocks() >= 20, "shared memory budget: K = 1280 must fit");
 };
 
 template <int FMT>
@@ -487,22 +493,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       if (!mbar_wait(&dfull[buf], (n_it / T::NDB) & 1, abort_flag)) break;
       tc_fence_after();
+      uint16_t* ystage = reinterpret_cast<uint16_t*>(smem + S::Y_OFF);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float acc[16];
         tmem_ld16(tmem_base + lane_base + T::D_COL + buf * BN + c0, acc);
         tc_wait_ld();
-        if (row_ok) {
+        if (!P.out_f32) {
+          store_slab_bf16(acc, gsc, bval, r, ystage + ((c0 / 16) & 1) * 16 * kRows, pr.y, pr.M, pr.N, m0 + c0,
+                          (int64_t)ic.nt * kRows);
+        } else if (row_ok) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
-            if (m < pr.M) {
-              const float val = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
-              if (P.out_f32)
-                reinterpret_cast<float*>(pr.y)[(int64_t)m * pr.N + n] = val;
-              else
-                reinterpret_cast<__nv_bfloat16*>(pr.y)[(int64_t)m * pr.N + n] = __float2bfloat16_rn(val);
-            }
+            if (m < pr.M)
+              reinterpret_cast<float*>(pr.y)[(int64_t)m * pr.N + n] = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
           }
         }
       }
@@ -576,7 +581,7 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::total(kMaxChunks));
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::total(S::max_blocks()));
   });
   if (attr_err != cudaSuccess) return WQ_ERR_CUDA;
 
@@ -659,6 +664,7 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   }
   int max_blocks = 1;
   for (int j = 0; j < count; ++j) max_blocks = std::max(max_blocks, P.prob[j].K / 64);
+  if (max_blocks > S::max_blocks()) return WQ_ERR_SHAPE;  // callers pick a configuration that fits
   P.sc_bytes = S::sc_bytes(max_blocks);
 
   cudaLaunchConfig_t cfg = {};
@@ -696,12 +702,27 @@ int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_st
     return launch_tcp<16, decode_stages(FMT), FMT, 256, rep, mode>(probs, count, out_f32, weights_static, s);
   }
   // GEMM: 256 activation rows per tile (N = 256 MMAs, one TMEM accumulator) where shared memory
-  // allows two stages of them; 128 rows (two accumulators) for q4_0 / q8_0
-  if constexpr (FMT == WQ_NVFP4)
-    return launch_tcp<256, 2, FMT, 128, 0, kScaleBF16>(probs, count, out_f32, weights_static, s);
-  if constexpr (FMT == WQ_NF4)
-    return launch_tcp<256, 2, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
-  return launch_tcp<128, kGemmStagesP, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
+  // allows two stages of them and the scale slices of the longest K; else 128 rows (two accumulators)
+  int64_t maxK = 0;
+  for (int i = 0; i < count; ++i) maxK = std::max(maxK, probs[i].K);
+  if constexpr (FMT == WQ_NVFP4) {
+    using Wide = PSmem<256, 2, FMT, 128, 0, kScaleBF16>;
+    if (maxK <= 64 * Wide::max_blocks())
+      return launch_tcp<256, 2, FMT, 128, 0, kScaleBF16>(probs, count, out_f32, weights_static, s);
+    using Deep = PSmem<128, kGemmStagesP, FMT, 128, 0, kScaleBF16>;
+    if (maxK <= 64 * Deep::max_blocks())
+      return launch_tcp<128, kGemmStagesP, FMT, 128, 0, kScaleBF16>(probs, count, out_f32, weights_static, s);
+    return launch_tcp<128, 2, FMT, 128, 0, kScaleBF16>(probs, count, out_f32, weights_static, s);
+  }
+  if constexpr (FMT == WQ_NF4) {
+    using Wide = PSmem<256, 2, FMT, 128, 1, kScaleF32>;
+    if (maxK <= 64 * Wide::max_blocks())
+      return launch_tcp<256, 2, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
+  }
+  using Deep = PSmem<128, kGemmStagesP, FMT, 128, 1, kScaleF32>;
+  if (maxK <= 64 * Deep::max_blocks())
+    return launch_tcp<128, kGemmStagesP, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
+  return launch_tcp<128, 2, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
 }
 
 }  // namespace

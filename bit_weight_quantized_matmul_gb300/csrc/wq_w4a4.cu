@@ -12,8 +12,8 @@
 // per-16 E4M3 block scales, which are held in tensor memory.  Nothing is decoded.
 //
 // Persistent CTA per SM over (weight tile, activation tile) items, warp-specialised:
-//   warp 0      TMA: W codes [128 x 256], x codes [128 x 256], both tiles' scales
-//   warp 1      TMEM owner, MMA issuer (4 MMAs of K = 64 per 256-element chunk)
+//   warp 0      TMA: W codes [128 x 512], x codes [128 x 512], both tiles' scales
+//   warp 1      TMEM owner, MMA issuer (8 MMAs of K = 64 per 512-element chunk)
 //   warps 2..5  scale warps: chunk scales smem -> TMEM (replicated 32-lane layout)
 //   warps 6..9  epilogue: tcgen05.ld, * g_x * g_w, + bias, store y
 // D is double-buffered in TMEM so an item's epilogue overlaps the next main loop.
@@ -26,17 +26,48 @@
 
 #include "wq_device.cuh"
 #include "wq_internal.h"
+#include "wq_tc_common.cuh"
 
 namespace wq {
 namespace {
 
 constexpr int kRows = 128;    // weight rows per tile (MMA M) == activation rows per tile (MMA N)
-constexpr int kKC = 256;      // K elements per chunk (one 128-byte row of packed codes)
-constexpr int kStages = 5;
 constexpr int kSFSlots = 4;   // TMEM scale ring
 constexpr int kThreads = 320;
-constexpr int kCodeBytes = kRows * kKC / 2;  // 16 KB per operand per chunk
-constexpr int kSFBytes = kRows * kKC / 16;   // 2 KB per operand per chunk
+
+// KC: K elements per chunk, 256 or 512 (one or two 128-byte swizzle rows of packed codes)
+template <int KC>
+struct Geo {
+  static constexpr int kKC = KC;
+  static constexpr int kSub = KC / 256;               // TMA boxes per operand per chunk
+  static constexpr int kStages = KC == 512 ? 3 : 5;
+  static constexpr int kCodeBytes = kRows * KC / 2;   // per operand per chunk
+  static constexpr int kSFBytes = kRows * KC / 16;    // per operand per chunk
+  static constexpr int kSFCols = 2 * 4 * (KC / 64);   // TMEM scale columns per chunk (both operands)
+};
+
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_st_cols<16>(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_cols<32>(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
 
 struct W4Params {
   const uint8_t* w_scales;   // weight scales blob (E4M3 [N, K/16] | pad | g)
@@ -52,7 +83,9 @@ struct W4Maps {
   CUtensorMap wc, xc, ws, xs;  // codes and scale maps of W and x
 };
 
+template <int KC>
 struct Lay {
+  static constexpr int kStages = Geo<KC>::kStages, kCodeBytes = Geo<KC>::kCodeBytes, kSFBytes = Geo<KC>::kSFBytes;
   static constexpr int A_OFF = 0;                              // W codes  [stage]
   static constexpr int B_OFF = A_OFF + kStages * kCodeBytes;   // x codes  [stage]
   static constexpr int SA_OFF = B_OFF + kStages * kCodeBytes;  // W scales [stage]
@@ -60,17 +93,24 @@ struct Lay {
   static constexpr int BAR_OFF = SB_OFF + kStages * kSFBytes;
   static constexpr int NBAR = 2 * kStages + 2 * kSFSlots + 4;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int TOTAL = MISC_OFF + 16 + 1024;
+  static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;  // [2] 4 KB output slabs
+  static constexpr int TOTAL = Y_OFF + 2 * 16 * kRows * 2 + 1024;
   static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
-// TMEM columns: D double buffer [0, 256), scale ring [256, 256 + 4 * 32)
+// TMEM columns: D double buffer [0, 256), scale ring [256, 256 + 4 * 64): per chunk 8 MMAs x
+// (4 columns of weight scales + 4 of activation scales)
 constexpr int kDCol = 0;
 constexpr int kSFCol = 2 * kRows;
 constexpr int kTmemCols = 512;
+static_assert(kSFCol + kSFSlots * Geo<512>::kSFCols <= kTmemCols, "TMEM budget");
 
+template <int KC>
 __global__ void __launch_bounds__(kThreads, 1)
     wq_w4a4_kernel(const __grid_constant__ W4Maps maps, const __grid_constant__ W4Params p) {
+  using Lay = wq::Lay<KC>;
+  constexpr int kKC = KC, kSub = Geo<KC>::kSub, kStages = Geo<KC>::kStages;
+  constexpr int kCodeBytes = Geo<KC>::kCodeBytes, kSFBytes = Geo<KC>::kSFBytes, kSFCols = Geo<KC>::kSFCols;
   constexpr uint32_t IDESC = idesc_nvf4(kRows, kRows);
   constexpr uint32_t STAGE_TX = 2 * kCodeBytes + 2 * kSFBytes;
   extern __shared__ uint8_t smem_raw[];
@@ -100,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   griddep_launch_dependents();
 
-  const int nch = p.K / kKC;
+  // a last chunk that runs past K reads TMA's zero fill: zero codes with zero scales add nothing
+  const int nch = (p.K + kKC - 1) / kKC;
   const int total = p.total_items;
   if (warp == 0) {
     // ---------------------------------------------- TMA producer
@@ -118,8 +159,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = g % kStages;
           if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], STAGE_TX);
-          tma_load_2d(smem + Lay::A_OFF + s * kCodeBytes, &maps.wc, &full[s], c * (kKC / 2), nt * kRows);
-          tma_load_2d(smem + Lay::B_OFF + s * kCodeBytes, &maps.xc, &full[s], c * (kKC / 2), mt * kRows);
+#pragma unroll
+          for (int b = 0; b < kSub; ++b) {  // [128 rows x 128 B] boxes, 128-byte swizzle
+            tma_load_2d(smem + Lay::A_OFF + s * kCodeBytes + b * 16384, &maps.wc, &full[s], c * (kKC / 2) + b * 128,
+                        nt * kRows);
+            tma_load_2d(smem + Lay::B_OFF + s * kCodeBytes + b * 16384, &maps.xc, &full[s], c * (kKC / 2) + b * 128,
+                        mt * kRows);
+          }
           tma_load_2d(smem + Lay::SA_OFF + s * kSFBytes, &maps.ws, &full[s], c * (kKC / 16), nt * kRows);
           tma_load_2d(smem + Lay::SB_OFF + s * kSFBytes, &maps.xs, &full[s], c * (kKC / 16), mt * kRows);
         }
@@ -144,10 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_s = smem_u32(smem + Lay::B_OFF + s * kCodeBytes);
 #pragma unroll
           for (int i = 0; i < kKC / 64; ++i) {  // K = 64 E2M1 values (32 bytes) per MMA
-            const uint64_t ad = smem_desc(a_s + i * 32, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b_s + i * 32, 16, 1024, 2);
-            const uint32_t sfa = tmem_base + kSFCol + slot * 32 + i * 4;
-            const uint32_t sfb = sfa + 16;
+            const uint32_t off = (i / 4) * 16384 + (i % 4) * 32;
+            const uint64_t ad = smem_desc(a_s + off, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b_s + off, 16, 1024, 2);
+            const uint32_t sfa = tmem_base + kSFCol + slot * kSFCols + i * 4;
+            const uint32_t sfb = sfa + kSFCols / 2;
             mma_nvf4_ss(d_tmem, ad, bd, IDESC, sfa, sfb, (c | i) != 0 ? 1u : 0u);
           }
           tc_commit(&sfempty[slot]);
@@ -157,12 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 6) {
-    // ---------------------------------------------- scale warps: smem [128 rows x 16 B] -> TMEM
-    // For MMA i of a chunk, lane r of every 32-lane quarter holds, in column j (j = 0..3), the
-    // four E4M3 scales (K blocks 4i .. 4i+3) of row 32 j + r -- the replicated layout that a
-    // 32x128b.warpx4 copy of a 512-byte scale atom produces.
+    // ---------------------------------------------- scale warps: smem [128 rows x KC/16 B] -> TMEM
+    // For MMA i of a chunk, lane r of every 32-lane quarter holds, in column 4 i + j (j = 0..3),
+    // the four E4M3 scales (K blocks 4i .. 4i+3) of row 32 j + r -- the replicated layout that a
+    // 32x128b.warpx4 copy of a 512-byte scale atom produces.  Each thread reads its four rows'
+    // scale bytes as 16-byte vectors and writes a whole chunk's columns with one store per operand.
     const int q = warp & 3;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    constexpr int NW = kKC / 64;  // 32-bit scale words per row per chunk (one per MMA)
     int g = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
@@ -170,18 +219,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = g % kStages, slot = g % kSFSlots;
         if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag)) { ok = false; break; }
         if (g >= kSFSlots && !mbar_wait(&sfempty[slot], ((g / kSFSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        const uint8_t* sa = smem + Lay::SA_OFF + s * kSFBytes;
-        const uint8_t* sb = smem + Lay::SB_OFF + s * kSFBytes;
 #pragma unroll
-        for (int i = 0; i < kKC / 64; ++i) {
-          uint32_t va[4], vb[4];
+        for (int op = 0; op < 2; ++op) {
+          const uint8_t* sbase = smem + (op == 0 ? Lay::SA_OFF : Lay::SB_OFF) + s * kSFBytes;
+          uint32_t v[4 * NW];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            va[j] = *reinterpret_cast<const uint32_t*>(sa + (32 * j + lane) * 16 + 4 * i);
-            vb[j] = *reinterpret_cast<const uint32_t*>(sb + (32 * j + lane) * 16 + 4 * i);
+            const uint4* row = reinterpret_cast<const uint4*>(sbase + (32 * j + lane) * (kKC / 16));
+#pragma unroll
+            for (int h = 0; h < NW / 4; ++h) {
+              const uint4 w = row[h];
+              v[(4 * h + 0) * 4 + j] = w.x;
+              v[(4 * h + 1) * 4 + j] = w.y;
+              v[(4 * h + 2) * 4 + j] = w.z;
+              v[(4 * h + 3) * 4 + j] = w.w;
+            }
           }
-          tmem_st<4>(tmem_base + lane_base + kSFCol + slot * 32 + i * 4, va);
-          tmem_st<4>(tmem_base + lane_base + kSFCol + slot * 32 + 16 + i * 4, vb);
+          tmem_st_cols<4 * NW>(tmem_base + lane_base + kSFCol + slot * kSFCols + op * (kSFCols / 2), v);
         }
         tc_wait_st();
         tc_fence_before();
@@ -207,22 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&dfull[buf], (n_it >> 1) & 1, abort_flag)) break;
       tc_fence_after();
       const int m0 = mt * kRows;
+      uint16_t* ystage = reinterpret_cast<uint16_t*>(smem + Lay::Y_OFF);
 #pragma unroll 1
       for (int c0 = 0; c0 < kRows; c0 += 16) {
         float acc[16];
         tmem_ld16(tmem_base + lane_base + kDCol + buf * kRows + c0, acc);
         tc_wait_ld();
-        if (row_ok) {
+        if (!p.out_f32) {
+          tc::store_slab_bf16(acc, gs, bval, r, ystage + ((c0 / 16) & 1) * 16 * kRows, p.y, p.M, p.N, m0 + c0,
+                              (int64_t)nt * kRows);
+        } else if (row_ok) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
-            if (m < p.M) {
-              const float val = __fadd_rn(__fmul_rn(acc[j], gs), bval);
-              if (p.out_f32)
-                reinterpret_cast<float*>(p.y)[(int64_t)m * p.N + n] = val;
-              else
-                reinterpret_cast<__nv_bfloat16*>(p.y)[(int64_t)m * p.N + n] = __float2bfloat16_rn(val);
-            }
+            if (m < p.M) reinterpret_cast<float*>(p.y)[(int64_t)m * p.N + n] = __fadd_rn(__fmul_rn(acc[j], gs), bval);
           }
         }
       }
@@ -252,26 +304,25 @@ int num_sms_w4() {
   return n;
 }
 
-}  // namespace
-
-int linear_w4a4_tc(const LinearArgs& a, cudaStream_t s, int* rc) {
-  // size rules: 256-element chunks with 16-byte scale rows; decode-sized M stays on the CUDA cores
-  if (a.M <= 16 || a.K % kKC != 0 || a.M > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF) return 0;
+template <int KC>
+int launch_w4a4(const LinearArgs& a, cudaStream_t s, int* rc) {
+  using Lay = wq::Lay<KC>;
+  auto kern = wq_w4a4_kernel<KC>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(wq_w4a4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL);
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL);
   });
   if (attr_err != cudaSuccess) { *rc = WQ_ERR_CUDA; return 1; }
   alignas(64) W4Maps maps;
   const uint64_t kb = (uint64_t)a.K / 2, ks = (uint64_t)a.K / 16;
-  bool ok = encode_tmap_2d(&maps.wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, kb, (uint64_t)a.N, kb, kKC / 2, kRows,
+  bool ok = encode_tmap_2d(&maps.wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, kb, (uint64_t)a.N, kb, 128, kRows,
                            CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_tmap_2d(&maps.xc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act_codes, kb, (uint64_t)a.M, kb, kKC / 2,
+            encode_tmap_2d(&maps.xc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act_codes, kb, (uint64_t)a.M, kb, 128,
                            kRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_tmap_2d(&maps.ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, ks, (uint64_t)a.N, ks, kKC / 16, kRows,
+            encode_tmap_2d(&maps.ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, ks, (uint64_t)a.N, ks, KC / 16, kRows,
                            CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_tmap_2d(&maps.xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act_scales, ks, (uint64_t)a.M, ks, kKC / 16,
+            encode_tmap_2d(&maps.xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act_scales, ks, (uint64_t)a.M, ks, KC / 16,
                            kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) { *rc = WQ_ERR_CUDA; return 1; }
   W4Params p;
@@ -301,10 +352,19 @@ int linear_w4a4_tc(const LinearArgs& a, cudaStream_t s, int* rc) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, wq_w4a4_kernel, maps, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, p);
   count_launch();
   *rc = e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
   return 1;
+}
+
+}  // namespace
+
+int linear_w4a4_tc(const LinearArgs& a, cudaStream_t s, int* rc) {
+  // size rules: scale rows of a multiple of 16 bytes (K % 256 == 0); decode-sized M stays on the CUDA cores
+  if (a.M <= 16 || a.K % 256 != 0 || a.M > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF) return 0;
+  // 512-element chunks when they tile K exactly, else 256
+  return a.K % 512 == 0 ? launch_w4a4<512>(a, s, rc) : launch_w4a4<256>(a, s, rc);
 }
 
 int take_status_w4a4() {

@@ -81,6 +81,7 @@ GEMM_SHAPES = [
     (300, 5120, 1280),                  # fc1 shape, ragged M
     (37, 1280, 5120),                   # fc2 shape, M between the decode and GEMM tiles
     (130, 200, 256),                    # ragged everything
+    (600, 640, 5120),                   # fc2's K with many activation tiles (the longest-K configuration)
 ]
 
 
@@ -131,7 +132,7 @@ def test_m_zero_is_noop():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("M,K", [(128, 256), (300, 512)])
+@pytest.mark.parametrize("M,K", [(128, 256), (300, 512), (200, 1280)])
 def test_w4a4_tensor_path_is_exact_products(M, K):
     """W4A4 on the block-scaled FP4 tensor cores: every product e2m1 * e4m3 * e2m1 * e4m3 is exact
     in fp32, so the fp32 output differs from the fp64 oracle only by the accumulation order and the
