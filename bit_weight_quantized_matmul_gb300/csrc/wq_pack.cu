@@ -184,23 +184,41 @@ __global__ void nf4_codes_kernel(const float* __restrict__ W, int64_t nb, uint8_
 }
 
 // ------------------------------------------------------------------ NVFP4
-template <typename T>
-__device__ __forceinline__ float load_as_f32(const T* p, int64_t i);
-template <>
-__device__ __forceinline__ float load_as_f32<float>(const float* p, int64_t i) { return p[i]; }
-template <>
-__device__ __forceinline__ float load_as_f32<uint16_t>(const uint16_t* p, int64_t i) {
-  return bf16_bits_to_f32(p[i]);
+// Eight consecutive values (index i, i % 8 == 0) as fp32, with 16-byte vector loads.
+__device__ __forceinline__ void load8_f32(const float* p, int64_t i, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p + i)[0], b = reinterpret_cast<const float4*>(p + i)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8_f32(const uint16_t* p, int64_t i, float (&v)[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p + i);
+  const uint32_t u[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = bf16_bits_to_f32(u[j] & 0xFFFFu);
+    v[2 * j + 1] = bf16_bits_to_f32(u[j] >> 16);
+  }
 }
 
-// amax over n values -> atomicMax on the bit pattern (non-negative floats order as integers)
+// amax over n values (n % 8 == 0) -> atomicMax on the bit pattern (non-negative floats order as integers)
 template <typename T>
 __global__ void amax_kernel(const T* __restrict__ X, int64_t n, unsigned* __restrict__ slot) {
   float a = 0.0f;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-    a = fmaxf(a, fabsf(load_as_f32(X, i)));
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < n; i += (int64_t)gridDim.x * blockDim.x * 8) {
+    float v[8];
+    load8_f32(X, i, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(v[j]));
+  }
+  // block maximum first, then one atomic per block
+  __shared__ unsigned wmax[32];
   unsigned u = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(a));
-  if ((threadIdx.x & 31) == 0 && u) atomicMax(slot, u);
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = u;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    u = (threadIdx.x < (blockDim.x >> 5)) ? wmax[threadIdx.x] : 0u;
+    u = __reduce_max_sync(0xFFFFFFFFu, u);
+    if (threadIdx.x == 0 && u) atomicMax(slot, u);
+  }
 }
 
 __device__ __forceinline__ float nvfp4_g_from_amax(float amax) {
@@ -220,11 +238,15 @@ __global__ void nvfp4_quant_kernel(const T* __restrict__ X, int64_t nblk, const 
   if (b >= nblk) return;
   float v[kNVBlock];
   float amax = 0.0f;
+  {
+    float lo[8], hi[8];
+    load8_f32(X, b * kNVBlock, lo);
+    load8_f32(X, b * kNVBlock + 8, hi);
 #pragma unroll
-  for (int i = 0; i < kNVBlock; ++i) {
-    v[i] = load_as_f32(X, b * kNVBlock + i);
-    amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < 8; ++i) { v[i] = lo[i]; v[i + 8] = hi[i]; }
   }
+#pragma unroll
+  for (int i = 0; i < kNVBlock; ++i) amax = fmaxf(amax, fabsf(v[i]));
   const uint32_t s = f32_to_e4m3_satfinite(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
   const float S = __fmul_rn(e4m3_to_f32(s), g);
   uint32_t lo = 0, hi = 0;
@@ -380,8 +402,8 @@ int pack_nvfp4(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* s
   const ScalesLayout lay = scales_layout(WQ_NVFP4, N, K);
   float* slot = reinterpret_cast<float*>(scales + lay.g_off);
   if (cudaMemsetAsync(slot, 0, sizeof(float), s) != cudaSuccess) return WQ_ERR_CUDA;
-  int g = grid_for(n, 256);
-  if (g > 4096) g = 4096;
+  int g = grid_for(n / 8, 256);
+  if (g > 304) g = 304;  // about two blocks per SM, each looping; one atomic per block
   amax_kernel<float><<<g, 256, 0, s>>>(W, n, reinterpret_cast<unsigned*>(slot));
   nvfp4_quant_kernel<float><<<grid_for(nblk, 256), 256, 0, s>>>(W, nblk, slot, 1, packed, scales, nullptr);
   nvfp4_finalize_kernel<<<1, 32, 0, s>>>(slot, scales + lay.sf_bytes, (int)(lay.g_off - lay.sf_bytes));
@@ -425,8 +447,8 @@ int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, 
     return launch_status();
   }
   if (cudaMemsetAsync(g_out, 0, sizeof(float), s) != cudaSuccess) return WQ_ERR_CUDA;
-  int g = grid_for(n, 256);
-  if (g > 4096) g = 4096;
+  int g = grid_for(n / 8, 256);
+  if (g > 304) g = 304;
   amax_kernel<uint16_t><<<g, 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(g_out));
   nvfp4_quant_kernel<uint16_t><<<grid_for(nblk, 256), 256, 0, s>>>(x, nblk, g_out, 1, codes, scales, nullptr);
   nvfp4_finalize_kernel<<<1, 32, 0, s>>>(g_out, nullptr, 0);
