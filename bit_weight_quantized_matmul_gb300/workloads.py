@@ -43,13 +43,14 @@ def _mix64(z):
 def splitmix64_next(seed):
     """Successor of a seed in a seed chain (one splitmix64 step)."""
     with np.errstate(over="ignore"):
-        s = np.array([seed], np.uint64) + GOLDEN
+        s = np.array([int(seed) % (1 << 64)], np.uint64) + GOLDEN
     return int(_mix64(s)[0])
 
 
 def raw_u64(seed, stream, n, start=0):
+    """n raw 64-bit values of stream (seed, stream), from counter start + 1 on (seeds are taken mod 2^64)."""
     with np.errstate(over="ignore"):
-        base = _mix64(np.array([seed], np.uint64) * GOLDEN + np.uint64(stream))[0]
+        base = _mix64(np.array([int(seed) % (1 << 64)], np.uint64) * GOLDEN + np.uint64(stream))[0]
         ctr = np.arange(start + 1, start + n + 1, dtype=np.uint64)
         return _mix64(base + ctr * GOLDEN)
 
