@@ -21,9 +21,16 @@
 //               row and half chunk, packed codes -> bf16 pairs -> tcgen05.st
 //               into a 4-slot TMEM ring.
 //   warps 10..13 epilogue: tcgen05.ld, x global scale (NVFP4), + bias, store y.
-//   warp 14     scale stager: one item ahead, copies the tile's per-(row, chunk)
-//               scale words into shared memory chunk-major (conflict-free reads;
-//               NF4's second-level decode q * s2 + offset is done here).
+//   warp 14     scale stager: one item ahead, bulk-copies the tile's scale slice
+//               into shared memory (NF4: also the tile's second-level scales).
+// Fold mode (decode) runs four MMA issuers instead of one: warps 1, 14, 15 and
+// 16, one per SM sub-partition, with the scale stager moved to warp 17.  One
+// thread issuing N <= 64 MMAs back to back gets about one per 45 cycles, and
+// far fewer when the table loads and TMEM stores of the dequant warps on its
+// sub-partition queue ahead of it; the tensor pipe itself takes an N = 16 MMA
+// in about 15 cycles.  Warps 1 and 14 issue the even chunks, 15 and 16 the odd
+// ones (each chunk's A slot and partial-tile slot are g & 1), and within a chunk
+// each issuer of the pair takes half of the scale blocks' partial tiles.
 // Every item covers the whole K range, so no cross-CTA reduction is needed.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -46,8 +53,13 @@ constexpr int kMaxItems = 2560;   // items a launch can schedule with an explici
 constexpr int kDeqQ = 2;          // dequant warps per TMEM lane quarter, each decoding 1/kDeqQ of a chunk
 constexpr int kDeqWarps = 4 * kDeqQ;
 constexpr int kEpiWarp0 = 2 + kDeqWarps;
-constexpr int kScaleWarp = kEpiWarp0 + 4;
-constexpr int kPThreads = (kScaleWarp + 1) * 32;  // 15 warps
+
+// Warps per CTA.  Fold mode adds three MMA issuers (warps 14, 15, 16) and moves the scale
+// stager to warp 17; the other modes run 15 warps (scale stager = warp 14).
+template <int MODE>
+constexpr int p_warps() { return MODE == 2 ? 18 : 15; }
+template <int MODE>
+constexpr int p_scale_warp() { return MODE == 2 ? 17 : 14; }
 constexpr int kMaxCtas = 160;     // persistent grid: one CTA per SM (152 on GB300)
 constexpr int kMaxChunks = 80;    // 64-element blocks per row: K <= 5120 on this path
 constexpr int kS2Max = 48;        // NF4: s2 values a tile can touch (128 * 80 / 256 + 2) + offset
@@ -95,8 +107,11 @@ struct PMaps {
 };
 static_assert(sizeof(PMaps) + sizeof(PParams) <= 32000, "kernel parameter space");
 
-template <int KC>
-constexpr int a_slots() { return KC == 256 ? 2 : 4; }  // TMEM A ring slots
+// TMEM A ring slots.  NF4 decode (fold mode, 64-blocks) fits a third 256-element slot
+// next to its partial-tile ring (3 x 128 + 2 x 4 x 16 = 512 columns), which lets the
+// dequant warps run a chunk further ahead of the MMAs.
+template <int KC, int FMT, int MODE>
+constexpr int a_slots() { return KC == 256 ? ((MODE == 2 && FMT == WQ_NF4) ? 3 : 2) : 4; }
 
 // Where the per-block weight scales are applied:
 //   kScaleF32   dequant warps multiply each code's value by its block scale in fp32
@@ -119,7 +134,7 @@ struct PSmem {
   static constexpr int LUT_OFF = W_OFF + STAGES * WB;
   static constexpr int LUT_BYTES = (FMT == WQ_Q8_0 || LUTREP == 0) ? 0 : 256 * (MODE == kScaleF32 ? 8 : 4) * LUTREP;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
-  static constexpr int NBAR = 2 * STAGES + 2 * a_slots<KC>() + 8;
+  static constexpr int NBAR = 2 * STAGES + 2 * a_slots<KC, FMT, MODE>() + 9;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;             // [2] 4 KB output slabs
   static constexpr int S2_OFF = Y_OFF + 2 * 16 * kRows * 2;                   // [2][kS2Max] NF4 s2 + offset
@@ -142,7 +157,7 @@ constexpr int scale_groups_per_128() { return FMT == WQ_NF4 ? 2 : FMT == WQ_NVFP
 
 template <int BN, int KC, int FMT, int MODE>
 struct PTmem {
-  static constexpr int NA = a_slots<KC>();
+  static constexpr int NA = a_slots<KC, FMT, MODE>();
   static constexpr int ACOLS = KC / 2;  // 32-bit columns per A slot (bf16 pairs)
   static constexpr int D_COL = NA * ACOLS;
   // kScaleFold: a double-buffered ring of per-scale-block partial tiles instead of D
@@ -171,7 +186,7 @@ __device__ __forceinline__ ItemCoord ItemIter::coord(const PParams& P) const {
 }
 
 template <int BN, int STAGES, int FMT, int KC, int LUTREP, int MODE>
-__global__ void __launch_bounds__(kPThreads, 1)
+__global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
     wq_tcp_kernel(const __grid_constant__ PMaps maps, const __grid_constant__ PParams P) {
   using S = PSmem<BN, STAGES, FMT, KC, LUTREP, MODE>;
   using T = PTmem<BN, KC, FMT, MODE>;
@@ -182,8 +197,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
   constexpr int kNA = T::NA;
   // fold warps read chunk g's partials once A slot g % NA is released, and the partial
   // ring is indexed g & 1: the two rings must coincide
-  static_assert(!FOLD || T::NA == 2, "fold mode pairs the partial ring with the A ring");
+  // the partial-tile ring has two slots (g & 1) whatever the A ring's depth
   constexpr int SCALE_CONSUMERS = FOLD ? 4 : kDeqWarps;
+  constexpr int NWARPS = p_warps<MODE>();
+  constexpr int SCALE_WARP = p_scale_warp<MODE>();
+  constexpr int NISSUE = FOLD ? 4 : 1;  // MMA issuers; fold mode: two per chunk
+  constexpr int CHUNK_COMMITS = FOLD ? 2 : 1;
   constexpr int SUB = S::SUB;
   constexpr int NE = KC / kDeqQ;  // elements of a row each dequant warp decodes per chunk
   static_assert(NE == 32 || NE % 64 == 0, "a dequant warp decodes half a 64-block or whole blocks");
@@ -204,6 +223,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* dempty = dfull + 2;    // [2]
   uint64_t* sfull = dempty + 2;    // [2]
   uint64_t* sempty = sfull + 2;    // [2]
+  uint64_t* done = sempty + 2;     // every warp has finished (TMEM may be released)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
   float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
@@ -212,10 +232,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
   float* s2buf = reinterpret_cast<float*>(smem + S::S2_OFF);
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
+  // MMA issuer index: warp 1 -> 0; fold mode also warps 14, 15, 16 -> 1, 2, 3
+  const int issuer = (warp == 1) ? 0 : (FOLD && warp >= 14 && warp <= 16) ? warp - 13 : -1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1 + kDeqWarps); }
-    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], 1); }
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], CHUNK_COMMITS + kDeqWarps); }
+    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], CHUNK_COMMITS); }
+    mbar_init(done, NWARPS);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&dfull[i], 1);   // kScaleFold: a partial-tile slot is full
       mbar_init(&dempty[i], 4);  // kScaleFold: a partial-tile slot was folded
@@ -226,7 +249,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     fence_mbar_init();
   }
   if (FMT != WQ_Q8_0 && LUTREP > 0) {
-    for (int i = threadIdx.x; i < 256 * LUTREP; i += kPThreads) {
+    for (int i = threadIdx.x; i < 256 * LUTREP; i += NWARPS * 32) {
       const uint32_t b = (uint32_t)(i / LUTREP);
       if (MODE == kScaleF32)
         lut[i] = make_float2(nibble_value<FMT>(b & 15u), nibble_value<FMT>(b >> 4));
@@ -289,55 +312,66 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer (whole warp waits, lane 0 issues)
+  } else if (issuer >= 0) {
+    // ------------------------------------------------ MMA issuers (whole warp waits, lane 0 issues)
     // A chunk's x tile is in shared memory once its A slot is full: every dequant warp waited
-    // for the stage's TMA transaction before it arrived on afull.
-    {
-      int g = 0, n_it = 0;
-      bool ok = true;
-      for (ItemIter ii(P); ii.more() && ok; ii.next(), ++n_it) {
-        const ItemCoord ic = ii.coord(P);
-        const int nch = (P.prob[ic.p].K + KC - 1) / KC;
-        const int buf = n_it % T::NDB;
-        if (!FOLD && !mbar_wait_lanes(&dempty[buf], ((n_it / T::NDB) & 1) ^ 1, lane == 0 && n_it >= T::NDB,
-                                      abort_flag))
-          break;
+    // for the stage's TMA transaction before it arrived on afull.  Fold mode: issuers 0 and 1
+    // take the even chunks, 2 and 3 the odd ones, and each issuer of a pair the partial tiles
+    // of half of the chunk's scale blocks; a commit tracks only its own thread's MMAs, so the
+    // A-slot and stage barriers expect one commit from each issuer of the pair.
+    const int pair = issuer >> 1, half = issuer & 1;
+    const uint64_t xdesc0 = smem_desc(smem_u32(smem + S::X_OFF), 16, 1024, 2);
+    int g = 0, n_it = 0;
+    bool ok = true;
+    for (ItemIter ii(P); ii.more() && ok; ii.next(), ++n_it) {
+      const ItemCoord ic = ii.coord(P);
+      const int nch = (P.prob[ic.p].K + KC - 1) / KC;
+      const int buf = n_it % T::NDB;
+      if (!FOLD && !mbar_wait_lanes(&dempty[buf], ((n_it / T::NDB) & 1) ^ 1, lane == 0 && n_it >= T::NDB,
+                                    abort_flag))
+        break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + T::D_COL + buf * BN;
+      for (int c = 0; c < nch; ++c, ++g) {
+        if (FOLD && (g & 1) != pair) continue;
+        const int s = g % STAGES, slot = g % kNA;
+        // lane 0: the A slot; lane 1 (fold mode): the partial-tile slot
+        uint64_t* wb = (lane == 0) ? &afull[slot] : &dempty[g & 1];
+        const uint32_t wp = (lane == 0) ? ((g / kNA) & 1) : (((g >> 1) & 1) ^ 1);
+        const bool act = (lane == 0) || (FOLD && lane == 1 && g >= 2);
+        if (!mbar_wait_lanes(wb, wp, act, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + T::D_COL + buf * BN;
-        for (int c = 0; c < nch; ++c, ++g) {
-          const int s = g % STAGES, slot = g % kNA;
-          // lane 0: the A slot; lane 1 (fold mode): the partial-tile slot
-          uint64_t* wb = (lane == 0) ? &afull[slot] : &dempty[g & 1];
-          const uint32_t wp = (lane == 0) ? ((g / kNA) & 1) : (((g >> 1) & 1) ^ 1);
-          const bool act = (lane == 0) || (FOLD && lane == 1 && g >= 2);
-          if (!mbar_wait_lanes(wb, wp, act, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t xaddr = smem_u32(smem + S::X_OFF + s * S::XB);
+        if (lane == 0) {
+          // descriptors as base + compile-time offsets (the 14-bit address field cannot
+          // carry: shared addresses stay below 2^18)
+          const uint64_t xdesc = xdesc0 + (uint64_t)((s * S::XB) >> 4);
+          const uint32_t a_tmem = tmem_base + slot * T::ACOLS;
+          if (FOLD) {
+            constexpr int KPG = (KC / 16) / T::G;  // MMA K steps per scale block
+            constexpr int GH = T::G / 2;           // scale blocks per issuer
+            const uint32_t p_tmem = tmem_base + T::D_COL + ((g & 1) * T::G + half * GH) * BN;
 #pragma unroll
-            for (int i = 0; i < KC / 16; ++i) {
-              if (FOLD) {
+            for (int step = 0; step < KPG; ++step)
+#pragma unroll
+              for (int gg = 0; gg < GH; ++gg) {
                 // consecutive MMAs go to different scale blocks' partial tiles
-                constexpr int KPG = (KC / 16) / T::G;  // MMA K steps per scale block
-                const int grp = i % T::G, step = i / T::G, kk = grp * KPG + step;
-                const uint64_t bdesc = smem_desc(xaddr + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024, 2);
-                const uint32_t p_tmem = tmem_base + T::D_COL + ((g & 1) * T::G + grp) * BN;
-                mma_bf16_ts(p_tmem, tmem_base + slot * T::ACOLS + kk * 8, bdesc, IDESC, step != 0 ? 1u : 0u);
-              } else {
-                const int kk = i;
-                const uint64_t bdesc = smem_desc(xaddr + (kk / 4) * BN * 128 + (kk % 4) * 32, 16, 1024, 2);
-                mma_bf16_ts(d_tmem, tmem_base + slot * T::ACOLS + kk * 8, bdesc, IDESC, (c | kk) != 0 ? 1u : 0u);
+                const int kk = (half * GH + gg) * KPG + step;
+                mma_bf16_ts(p_tmem + gg * BN, a_tmem + kk * 8, xdesc + (uint64_t)((kk / 4) * BN * 8 + (kk % 4) * 2),
+                            IDESC, step != 0 ? 1u : 0u);
               }
-            }
-            tc_commit(&aempty[slot]);
-            tc_commit(&empty[s]);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < KC / 16; ++kk)
+              mma_bf16_ts(d_tmem, a_tmem + kk * 8, xdesc + (uint64_t)((kk / 4) * BN * 8 + (kk % 4) * 2), IDESC,
+                          (c | kk) != 0 ? 1u : 0u);
           }
-          __syncwarp();
+          tc_commit(&aempty[slot]);
+          tc_commit(&empty[s]);
         }
-        if (ok && !FOLD && lane == 0) tc_commit(&dfull[buf]);
         __syncwarp();
       }
+      if (ok && !FOLD && lane == 0) tc_commit(&dfull[buf]);
+      __syncwarp();
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------ dequant warps: half h of every chunk
@@ -409,7 +443,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       __syncwarp();
       if (!FOLD && lane == 0) mbar_arrive(&sempty[sb]);
     }
-  } else if (warp < kScaleWarp) {
+  } else if (warp < kEpiWarp0 + 4) {
     // ------------------------------------------------ epilogue warps
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -515,7 +549,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&dempty[buf]);
     }
-  } else {
+  } else if (warp == SCALE_WARP) {
     // ------------------------------------------------ scale warp: one item ahead of the dequant warps,
     // one bulk copy of the tile's scale slice (contiguous in the blob) into shared memory
     int n_it = 0;
@@ -554,10 +588,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
   }
 
+  // Teardown: every warp arrives once its own work is over (its MMAs waited for by the
+  // fold / epilogue warps, its TMEM stores and loads waited for); warp 1 releases TMEM after
+  // all arrivals.  An mbarrier with an explicit count, not a CTA-wide bar.sync, so that no
+  // lane-divergent path of a warp-specialised role can complete it early.
   tc_fence_before();
   __syncwarp();
-  __syncthreads();
+  if (lane == 0) mbar_arrive(done);
   if (warp == 1) {
+    // bounded, and not cut short by the abort flag: every other wait is bounded, so every
+    // warp arrives; TMEM is released in any case before the CTA exits
+    for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(done, 0); ++i) {
+    }
     tc_fence_after();
     tmem_dealloc(tmem_base, T::ALLOC);
   }
@@ -669,7 +711,7 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kPThreads, 1, 1);
+  cfg.blockDim = dim3(p_warps<MODE>() * 32, 1, 1);
   cfg.dynamicSmemBytes = S::total(max_blocks);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
