@@ -134,7 +134,7 @@ struct PSmem {
   static constexpr int LUT_OFF = W_OFF + STAGES * WB;
   static constexpr int LUT_BYTES = (FMT == WQ_Q8_0 || LUTREP == 0) ? 0 : 256 * (MODE == kScaleF32 ? 8 : 4) * LUTREP;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
-  static constexpr int NBAR = 2 * STAGES + 2 * a_slots<KC, FMT, MODE>() + 9;
+  static constexpr int NBAR = 3 * STAGES + 2 * a_slots<KC, FMT, MODE>() + 9;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;             // [2] 4 KB output slabs
   static constexpr int S2_OFF = Y_OFF + 2 * 16 * kRows * 2;                   // [2][kS2Max] NF4 s2 + offset
@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   constexpr int NE = KC / kDeqQ;  // elements of a row each dequant warp decodes per chunk
   static_assert(NE == 32 || NE % 64 == 0, "a dequant warp decodes half a 64-block or whole blocks");
   constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
-  constexpr uint32_t STAGE_TX = (uint32_t)(S::XB + S::WB);
   constexpr int WCHUNK = Fmt<FMT>::WB * SUB;  // packed bytes of one row per chunk
   constexpr int WRB = WCHUNK < 128 ? WCHUNK : 128;  // row bytes of one W TMA box (swizzle width)
   constexpr int WNBOX = WCHUNK / WRB;
@@ -215,7 +214,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
-  uint64_t* full = bars;
+  uint64_t* wfull = bars;           // [STAGES] a stage's weight tile has landed
   uint64_t* empty = bars + STAGES;
   uint64_t* afull = bars + 2 * STAGES;
   uint64_t* aempty = afull + kNA;
@@ -224,6 +223,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   uint64_t* sfull = dempty + 2;    // [2]
   uint64_t* sempty = sfull + 2;    // [2]
   uint64_t* done = sempty + 2;     // every warp has finished (TMEM may be released)
+  uint64_t* xfull = done + 1;      // [STAGES] a stage's activation tile has landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
   float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
@@ -236,7 +236,11 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   const int issuer = (warp == 1) ? 0 : (FOLD && warp >= 14 && warp <= 16) ? warp - 13 : -1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], CHUNK_COMMITS + kDeqWarps); }
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&xfull[i], 1);
+      mbar_init(&empty[i], CHUNK_COMMITS + kDeqWarps);
+    }
     for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], CHUNK_COMMITS); }
     mbar_init(done, NWARPS);
     for (int i = 0; i < 2; ++i) {
@@ -272,7 +276,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         prefetch_tmap(&maps.w[i]);
         prefetch_tmap(&maps.x[i]);
       }
-      // weights of the first STAGES chunks may stream before the preceding kernel finishes
+      // weights of the first STAGES chunks may stream (and be decoded) before the preceding
+      // kernel finishes; weights and activations have separate barriers, so only the MMAs
+      // wait for the activations
       int pre = 0;
       if (P.weights_static) {
         int g = 0;
@@ -280,9 +286,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
           const ItemCoord ic = ii.coord(P);
           const int nch = (P.prob[ic.p].K + KC - 1) / KC;
           for (int c = 0; c < nch && g < STAGES; ++c, ++g) {
-            mbar_arrive_expect_tx(&full[g], STAGE_TX);
+            mbar_arrive_expect_tx(&wfull[g], (uint32_t)S::WB);
             for (int b = 0; b < WNBOX; ++b)
-              tma_load_2d(smem + S::W_OFF + g * S::WB + b * 128 * WRB, &maps.w[ic.p], &full[g],
+              tma_load_2d(smem + S::W_OFF + g * S::WB + b * 128 * WRB, &maps.w[ic.p], &wfull[g],
                           c * WCHUNK + b * WRB, ic.nt * kRows);
           }
         }
@@ -300,22 +306,22 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
             // stage s is free once chunk g - STAGES is consumed (x by its MMAs, weights by the
             // dequant warps); a per-stage barrier cannot complete twice before this wait
             if (g >= STAGES && !mbar_wait(&empty[s], ((g / STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
-            mbar_arrive_expect_tx(&full[s], STAGE_TX);
+            mbar_arrive_expect_tx(&wfull[s], (uint32_t)S::WB);
             for (int b = 0; b < WNBOX; ++b)
-              tma_load_2d(smem + S::W_OFF + s * S::WB + b * 128 * WRB, &maps.w[ic.p], &full[s],
+              tma_load_2d(smem + S::W_OFF + s * S::WB + b * 128 * WRB, &maps.w[ic.p], &wfull[s],
                           c * WCHUNK + b * WRB, ic.nt * kRows);
           }
+          mbar_arrive_expect_tx(&xfull[s], (uint32_t)S::XB);
 #pragma unroll
           for (int j = 0; j < SUB; ++j)
-            tma_load_2d(smem + S::X_OFF + s * S::XB + j * BN * 128, &maps.x[ic.p], &full[s], c * KC + j * 64,
+            tma_load_2d(smem + S::X_OFF + s * S::XB + j * BN * 128, &maps.x[ic.p], &xfull[s], c * KC + j * 64,
                         ic.mt * BN);
         }
       }
     }
   } else if (issuer >= 0) {
     // ------------------------------------------------ MMA issuers (whole warp waits, lane 0 issues)
-    // A chunk's x tile is in shared memory once its A slot is full: every dequant warp waited
-    // for the stage's TMA transaction before it arrived on afull.  Fold mode: issuers 0 and 1
+    // Fold mode: issuers 0 and 1
     // take the even chunks, 2 and 3 the odd ones, and each issuer of a pair the partial tiles
     // of half of the chunk's scale blocks; a commit tracks only its own thread's MMAs, so the
     // A-slot and stage barriers expect one commit from each issuer of the pair.
@@ -335,10 +341,10 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       for (int c = 0; c < nch; ++c, ++g) {
         if (FOLD && (g & 1) != pair) continue;
         const int s = g % STAGES, slot = g % kNA;
-        // lane 0: the A slot; lane 1 (fold mode): the partial-tile slot
-        uint64_t* wb = (lane == 0) ? &afull[slot] : &dempty[g & 1];
-        const uint32_t wp = (lane == 0) ? ((g / kNA) & 1) : (((g >> 1) & 1) ^ 1);
-        const bool act = (lane == 0) || (FOLD && lane == 1 && g >= 2);
+        // lane 0: the A slot; lane 1 (fold mode): the partial-tile slot; lane 2: the x tile
+        uint64_t* wb = (lane == 0) ? &afull[slot] : (lane == 1) ? &dempty[g & 1] : &xfull[s];
+        const uint32_t wp = (lane == 0) ? ((g / kNA) & 1) : (lane == 1) ? (((g >> 1) & 1) ^ 1) : ((g / STAGES) & 1);
+        const bool act = (lane == 0) || (FOLD && lane == 1 && g >= 2) || (lane == 2);
         if (!mbar_wait_lanes(wb, wp, act, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
@@ -414,7 +420,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
             }
           }
         }
-        if (!mbar_wait(&full[s], (g / STAGES) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&wfull[s], (g / STAGES) & 1, abort_flag)) { ok = false; break; }
         if (g >= kNA && !mbar_wait(&aempty[slot], ((g / kNA) & 1) ^ 1, abort_flag)) { ok = false; break; }
         const uint8_t* wstage = smem + S::W_OFF + s * S::WB;
         constexpr int NES = NE / NBW;                          // elements per decode call (32 or 64)
