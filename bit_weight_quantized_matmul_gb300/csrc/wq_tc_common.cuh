@@ -257,6 +257,9 @@ __device__ __forceinline__ void decode_span_bf16(uint32_t sword, int part, const
     }
     return;
   }
+  // this lane's copy of the table, addressed in bytes: one byte-permute and one shifted add
+  // per packed byte
+  const uint8_t* lbase = reinterpret_cast<const uint8_t*>(lut + lsel);
 #pragma unroll
   for (int q = 0; q < NE / 32; ++q) {
     const uint4 v = wv[q];
@@ -271,7 +274,8 @@ __device__ __forceinline__ void decode_span_bf16(uint32_t sword, int part, const
       }
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint32_t pair = lut[((u[j] >> (8 * b)) & 0xFFu) * LUTREP + lsel];
+        const uint32_t byte = __byte_perm(u[j], 0u, 0x4440u + (uint32_t)b);
+        const uint32_t pair = *reinterpret_cast<const uint32_t*>(lbase + byte * (uint32_t)(LUTREP * 4));
         out[q * 16 + j * 4 + b] = SCALED ? hmul2_bf16(pair, spair) : pair;
       }
     }

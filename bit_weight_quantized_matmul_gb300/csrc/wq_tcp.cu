@@ -23,14 +23,13 @@
 //   warps 10..13 epilogue: tcgen05.ld, x global scale (NVFP4), + bias, store y.
 //   warp 14     scale stager: one item ahead, bulk-copies the tile's scale slice
 //               into shared memory (NF4: also the tile's second-level scales).
-// Fold mode (decode) runs four MMA issuers instead of one: warps 1, 14, 15 and
-// 16, one per SM sub-partition, with the scale stager moved to warp 17.  One
-// thread issuing N <= 64 MMAs back to back gets about one per 45 cycles, and
-// far fewer when the table loads and TMEM stores of the dequant warps on its
-// sub-partition queue ahead of it; the tensor pipe itself takes an N = 16 MMA
-// in about 15 cycles.  Warps 1 and 14 issue the even chunks, 15 and 16 the odd
-// ones (each chunk's A slot and partial-tile slot are g & 1), and within a chunk
-// each issuer of the pair takes half of the scale blocks' partial tiles.
+// Fold mode (decode) runs four MMA issuers -- warps 1, 14, 15 and 16, one per SM
+// sub-partition -- and the scale stager on warp 17.  One thread issuing N <= 64 MMAs back to back gets about
+// one per 45 cycles, and far fewer when the table loads and TMEM stores of the
+// dequant warps on its sub-partition queue ahead of it; the tensor pipe itself
+// takes an N = 16 MMA in about 15 cycles.  Issuers 0 and 1 take the even chunks,
+// 2 and 3 the odd ones (the partial-tile slot is g & 1), and within a chunk each
+// issuer of the pair takes half of the scale blocks' partial tiles.
 // Every item covers the whole K range, so no cross-CTA reduction is needed.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -50,16 +49,20 @@ namespace {
 using namespace tc;
 
 constexpr int kMaxItems = 2560;   // items a launch can schedule with an explicit per-CTA list
-constexpr int kDeqQ = 2;          // dequant warps per TMEM lane quarter, each decoding 1/kDeqQ of a chunk
-constexpr int kDeqWarps = 4 * kDeqQ;
-constexpr int kEpiWarp0 = 2 + kDeqWarps;
 
-// Warps per CTA.  Fold mode adds three MMA issuers (warps 14, 15, 16) and moves the scale
-// stager to warp 17; the other modes run 15 warps (scale stager = warp 14).
+// Warp layout.  Every mode: warp 0 TMA producer, warp 1 MMA issuer, then the dequant warps
+// (kDeqQ per TMEM lane quarter, each decoding 1/kDeqQ of a chunk), then four epilogue / fold
+// warps.  The other modes end with the scale stager (15 warps); fold mode (decode) adds three
+// MMA issuers, one on each other SM sub-partition, before the scale stager (18 warps).  Four
+// dequant warps per quarter measured slower than two.
 template <int MODE>
-constexpr int p_warps() { return MODE == 2 ? 18 : 15; }
+constexpr int p_deq_q() { return 2; }
 template <int MODE>
-constexpr int p_scale_warp() { return MODE == 2 ? 17 : 14; }
+constexpr int p_epi_warp0() { return 2 + 4 * p_deq_q<MODE>(); }
+template <int MODE>
+constexpr int p_scale_warp() { return p_epi_warp0<MODE>() + (MODE == 2 ? 7 : 4); }
+template <int MODE>
+constexpr int p_warps() { return p_scale_warp<MODE>() + 1; }
 constexpr int kMaxCtas = 160;     // persistent grid: one CTA per SM (152 on GB300)
 constexpr int kMaxChunks = 80;    // 64-element blocks per row: K <= 5120 on this path
 constexpr int kS2Max = 48;        // NF4: s2 values a tile can touch (128 * 80 / 256 + 2) + offset
@@ -198,6 +201,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   // fold warps read chunk g's partials once A slot g % NA is released, and the partial
   // ring is indexed g & 1: the two rings must coincide
   // the partial-tile ring has two slots (g & 1) whatever the A ring's depth
+  constexpr int kDeqQ = p_deq_q<MODE>();
+  constexpr int kDeqWarps = 4 * kDeqQ;
+  constexpr int kEpiWarp0 = p_epi_warp0<MODE>();
   constexpr int SCALE_CONSUMERS = FOLD ? 4 : kDeqWarps;
   constexpr int NWARPS = p_warps<MODE>();
   constexpr int SCALE_WARP = p_scale_warp<MODE>();
@@ -233,7 +239,8 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
   // MMA issuer index: warp 1 -> 0; fold mode also warps 14, 15, 16 -> 1, 2, 3
-  const int issuer = (warp == 1) ? 0 : (FOLD && warp >= 14 && warp <= 16) ? warp - 13 : -1;
+  const int issuer =
+      (warp == 1) ? 0 : (FOLD && warp >= kEpiWarp0 + 4 && warp <= kEpiWarp0 + 6) ? warp - (kEpiWarp0 + 3) : -1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -736,7 +743,10 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
 
 // decode: 256-element chunks, lane-replicated bf16-pair table, block scales folded after the
 // MMA (NVFP4: exact bf16 scaling); GEMM: 128-element chunks, compact fp32 table
-constexpr int decode_stages(int fmt) { return fmt == WQ_Q8_0 ? 3 : 4; }
+// Decode is bound by the weight bytes in flight per SM: as many stages as shared memory holds
+// next to the scale slices of a K = 5120 tile (1 byte per row and 64-block for NF4, 4 for the
+// others; q8_0 stages are twice as large).
+constexpr int decode_stages(int fmt) { return fmt == WQ_NF4 ? 6 : fmt == WQ_Q8_0 ? 3 : 4; }
 constexpr int kGemmStagesP = 3;
 
 template <int FMT>
@@ -747,6 +757,8 @@ int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   if (maxM <= 16) {
     constexpr int mode = FMT == WQ_NVFP4 ? kScaleBF16 : kScaleFold;
     constexpr int rep = FMT == WQ_NVFP4 ? 0 : 32;
+    static_assert(PSmem<16, decode_stages(FMT), FMT, 256, rep, mode>::max_blocks() >= kMaxChunks,
+                  "decode tiles must take K = 5120");
     return launch_tcp<16, decode_stages(FMT), FMT, 256, rep, mode>(probs, count, out_f32, weights_static, s);
   }
   // GEMM: 256 activation rows per tile (N = 256 MMAs, one TMEM accumulator) where shared memory
