@@ -335,7 +335,8 @@ def load_traffic(kernel, workload):
 def extra_gemm(wq, wl, dev, peaks):
     """Encoder-side context (configs 2 and 3 shapes): the fc1 Linear (N=5120, K=1280) at
     M = 1500 x 4 in NVFP4 W4A16, and in W4A4 (GEMM alone, and with the runtime activation
-    quantiser); L2 flushed before every launch; median of 10."""
+    quantiser); each measured call is one CUDA graph (the quantiser's kernels and the GEMM
+    replay back to back); L2 flushed before every replay; median of 10."""
     import torch
     M, N, K = 6000, 5120, 1280
     W = torch.from_numpy(wl.weight(101, N, K)).to(dev)
@@ -351,12 +352,16 @@ def extra_gemm(wq, wl, dev, peaks):
     def timed(fn):
         for _ in range(3):
             fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
         ts = []
         for _ in range(10):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            fn()
+            g.replay()
             e1.record()
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1))
@@ -383,7 +388,8 @@ def run_encoder(args, rank, local_rank, world):
     """Configs 2 / 3: the encoder Linear shapes (q/k/v/o 1280x1280, fc1 5120x1280, fc2
     1280x5120) at M = 1500 x B for B in {1, 4, 16}, NVFP4 weights, bf16 activations with 0.1 %
     outliers x20; W4A16, or W4A4 with the runtime activation quantiser inside the step.  One step
-    = the 9 GEMMs; each launch is timed with CUDA events after an L2 flush (excluded)."""
+    = the 9 GEMMs; each GEMM (with its quantiser, for W4A4) is one CUDA graph replay, timed with
+    CUDA events after an L2 flush (excluded)."""
     import torch
     from bit_weight_quantized_matmul_gb300 import build as B
     B.build()
@@ -418,6 +424,11 @@ def run_encoder(args, rank, local_rank, world):
         for c in cases:
             launch(c)
     torch.cuda.synchronize()
+    for c in cases:
+        c["graph"] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(c["graph"]):
+            launch(c)
+    torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(len(cases) * args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -426,7 +437,7 @@ def run_encoder(args, rank, local_rank, world):
         for c in cases:
             flush.zero_()
             ev[k][0].record()
-            launch(c)
+            c["graph"].replay()
             ev[k][1].record()
             k += 1
     torch.cuda.synchronize()
@@ -448,7 +459,8 @@ def run_encoder(args, rank, local_rank, world):
             "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": ("W4A4 (activation quantiser in the step)" if w4a4 else "W4A16") +
                                    ": encoder Linears qkvo/fc1/fc2 at M=1500*B, B in {1,4,16} (9 GEMMs/step)",
-                       "l2": "flushed (256 MB write) before every launch, outside the timed events"},
+                       "l2": "flushed (256 MB write) before every launch, outside the timed events",
+                       "launch": "one CUDA graph replay per GEMM (W4A4: the quantiser's kernels and the GEMM)"},
             "roofline": {"bound": "tensor", "achieved": round(value / world, 2), "peak": pk * (4 if w4a4 else 1),
                          "unit": "TFLOP/s", "frac": round(value / world / (pk * (4 if w4a4 else 1)), 4),
                          "peak_source": src + (" bf16 x 4 (nominal fp4 ratio)" if w4a4 else ""), "traffic": None},

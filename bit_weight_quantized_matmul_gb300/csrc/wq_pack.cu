@@ -203,7 +203,20 @@ __device__ __forceinline__ void load8_f32(const uint16_t* p, int64_t i, float (&
 template <typename T>
 __global__ void amax_kernel(const T* __restrict__ X, int64_t n, unsigned* __restrict__ slot) {
   float a = 0.0f;
-  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < n; i += (int64_t)gridDim.x * blockDim.x * 8) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x * 8;
+  int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  // four independent 16-byte loads in flight per thread: the grid is capped at two CTAs per SM
+  for (; i + 3 * stride < n; i += 4 * stride) {
+    float v0[8], v1[8], v2[8], v3[8];
+    load8_f32(X, i, v0);
+    load8_f32(X, i + stride, v1);
+    load8_f32(X, i + 2 * stride, v2);
+    load8_f32(X, i + 3 * stride, v3);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      a = fmaxf(a, fmaxf(fmaxf(fabsf(v0[j]), fabsf(v1[j])), fmaxf(fabsf(v2[j]), fabsf(v3[j]))));
+  }
+  for (; i < n; i += stride) {
     float v[8];
     load8_f32(X, i, v);
 #pragma unroll
