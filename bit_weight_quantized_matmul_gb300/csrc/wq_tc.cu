@@ -54,7 +54,7 @@ struct Smem {
   static constexpr int W_OFF = X_OFF + STAGES * XB;
   static constexpr int LUT_OFF = W_OFF + STAGES * WB;  // 256 x float2
   static constexpr int BAR_OFF = LUT_OFF + 256 * 8;
-  static constexpr int NBAR = 2 * STAGES + 2 * kNA + 1;
+  static constexpr int NBAR = 2 * STAGES + 2 * kNA + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tmem base, abort flag
   static constexpr int RED_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
   static constexpr int RED_BYTES = (BN <= 16) ? kRows * (BN + 1) * 4 : 0;
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* afull = bars + 2 * STAGES;
   uint64_t* aempty = afull + kNA;
   uint64_t* dfull = aempty + kNA;
+  uint64_t* done = dfull + 1;  // every warp has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
   float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1 + 4); }
     for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], 4); mbar_init(&aempty[i], 1); }
     mbar_init(dfull, 1);
+    mbar_init(done, kThreads / 32);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -246,10 +248,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();
   }
 
+  // Teardown: an mbarrier counts every warp before warp 1 releases TMEM (bounded, and not cut
+  // short by the abort flag: every other wait is bounded, so every warp arrives).
   tc_fence_before();
   __syncwarp();
-  __syncthreads();
+  if (lane == 0) mbar_arrive(done);
   if (warp == 1) {
+    for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(done, 0); ++i) {
+    }
     tc_fence_after();
     tmem_dealloc(tmem_base, T::ALLOC);
   }

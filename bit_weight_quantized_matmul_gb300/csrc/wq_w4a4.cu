@@ -91,7 +91,7 @@ struct Lay {
   static constexpr int SA_OFF = B_OFF + kStages * kCodeBytes;  // W scales [stage]
   static constexpr int SB_OFF = SA_OFF + kStages * kSFBytes;   // x scales [stage]
   static constexpr int BAR_OFF = SB_OFF + kStages * kSFBytes;
-  static constexpr int NBAR = 2 * kStages + 2 * kSFSlots + 4;
+  static constexpr int NBAR = 2 * kStages + 2 * kSFSlots + 5;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;  // [2] 4 KB output slabs
   static constexpr int TOTAL = Y_OFF + 2 * 16 * kRows * 2 + 1024;
@@ -122,12 +122,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sfempty = sffull + kSFSlots;
   uint64_t* dfull = sfempty + kSFSlots;  // [2]
   uint64_t* dempty = dfull + 2;          // [2]
+  uint64_t* done = dempty + 2;           // every warp has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::MISC_OFF + 4);
   const int warp = (int)warp_id(), lane = (int)lane_id();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1 + 4); }
+    mbar_init(done, kThreads / 32);
     for (int i = 0; i < kSFSlots; ++i) { mbar_init(&sffull[i], 4); mbar_init(&sfempty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4); }
     *abort_flag = 0;
@@ -284,10 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Teardown: an mbarrier counts every warp (a CTA-wide bar.sync after lane-divergent roles is not
+  // relied on), then warp 1 releases TMEM.  The wait is bounded and not cut short by the abort
+  // flag: every other wait is bounded, so every warp arrives.
   tc_fence_before();
   __syncwarp();
-  __syncthreads();
+  if (lane == 0) mbar_arrive(done);
   if (warp == 1) {
+    for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(done, 0); ++i) {
+    }
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
