@@ -256,6 +256,11 @@ int wq_linear(const void* x, const void* packed, const void* scales, int fmt, in
   return wq_linear_ex(x, packed, scales, fmt, M, N, K, bias, y, 0u, stream);
 }
 
+int wq_selftest_timeout(uint32_t polls, void* stream) {
+  if (polls < 1 || polls > (1u << 20)) return WQ_ERR_ARG;
+  return wq::selftest_timeout(polls, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int wq_last_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
   int worst = WQ_OK;

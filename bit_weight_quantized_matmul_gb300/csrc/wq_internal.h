@@ -36,6 +36,7 @@ int dequant(const uint8_t* packed, const uint8_t* scales, int fmt, int64_t N, in
 int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, uint8_t* codes,
                     uint8_t* scales, float* g_out, cudaStream_t s);
 int take_status_pack();
+int selftest_timeout(uint32_t polls, cudaStream_t s);  // bounded wait on a barrier nobody arrives on
 
 // ---- linear: CUDA-core path (wq_simt.cu)
 struct LinearArgs {

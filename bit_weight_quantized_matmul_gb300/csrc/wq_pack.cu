@@ -450,6 +450,28 @@ int dequant(const uint8_t* packed, const uint8_t* scales, int fmt, int64_t N, in
   return launch_status();
 }
 
+// Failure-path self test: one thread waits on an mbarrier that nothing arrives on, with the
+// same bounded poll the pipelines use, and records WQ_STATUS_TIMEOUT once it gives up.
+__global__ void selftest_timeout_kernel(uint32_t polls) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t i = 0;
+    while (i < polls && !mbar_try_wait(&bar, 0)) ++i;
+    if (i == polls) set_status(WQ_STATUS_TIMEOUT);
+  }
+}
+
+int selftest_timeout(uint32_t polls, cudaStream_t s) {
+  selftest_timeout_kernel<<<1, 32, 0, s>>>(polls);
+  count_launch();
+  return launch_status();
+}
+
 int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, uint8_t* codes,
                     uint8_t* scales, float* g_out, cudaStream_t s) {
   const int64_t n = M * K, nblk = n / kNVBlock;

@@ -19,7 +19,7 @@
 //               main loop of the next.
 //   warps 2..9  dequant: two warps per TMEM lane quarter, one thread per weight
 //               row and half chunk, packed codes -> bf16 pairs -> tcgen05.st
-//               into a 4-slot TMEM ring.
+//               into a TMEM ring of 2 to 4 A slots.
 //   warps 10..13 epilogue: tcgen05.ld, x global scale (NVFP4), + bias, store y.
 //   warp 14     scale stager: one item ahead, bulk-copies the tile's scale slice
 //               into shared memory (NF4: also the tile's second-level scales).

@@ -55,6 +55,7 @@ _SIGS = {
     "wq_last_device_status": (_I, []),
     "wq_status_string": (ctypes.c_char_p, [_I]),
     "wq_kernel_launches": (ctypes.c_uint64, []),
+    "wq_selftest_timeout": (_I, [ctypes.c_uint32, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -188,3 +189,9 @@ def last_device_status():
 
 def kernel_launches():
     return int(lib.wq_kernel_launches())
+
+
+def selftest_timeout(polls=1000, stream=None):
+    """Run the bounded-wait failure path once (a barrier nobody arrives on); the next
+    last_device_status() reports WQ_ERR_TIMEOUT."""
+    _check("wq_selftest_timeout", lib.wq_selftest_timeout(polls, _stream(stream)))

@@ -188,6 +188,17 @@ int wq_last_device_status(void);
 const char* wq_status_string(int status);
 uint64_t wq_kernel_launches(void);
 
+/* ---------------------------------------------------------------- failure detection
+ * wq_selftest_timeout: launches one small kernel that waits, with the same
+ * bounded mbarrier poll every kernel of this library uses, on a barrier that
+ * nothing ever arrives on, giving up after `polls` polls (1 <= polls <= 2^20).
+ * The kernel then records WQ_ERR_TIMEOUT in the device status word and
+ * returns normally: no trap, the context stays usable.  A following
+ * wq_last_device_status() returns WQ_ERR_TIMEOUT (and clears it).  Exercises
+ * the path a real stall takes (a TMA transaction or a peer that never
+ * arrives) without faulting the GPU.  WQ_ERR_ARG for polls out of range.    */
+int wq_selftest_timeout(uint32_t polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -83,6 +83,9 @@ def test_argument_checks_before_any_launch(wq):
     act = wq.wq_act_nvfp4(0x10000, None, 0x10000)
     xp = ctypes.cast(ctypes.pointer(act), ctypes.c_void_p)
     assert L.wq_linear(xp, fake, fake, wq.WQ_NVFP4_W4A4, 1, 4, 64, None, fake, None) == wq.WQ_ERR_ARG
+    # the failure-path self test checks its poll count before launching
+    assert L.wq_selftest_timeout(0, None) == wq.WQ_ERR_ARG
+    assert L.wq_selftest_timeout((1 << 20) + 1, None) == wq.WQ_ERR_ARG
 
 
 def test_status_strings(wq):
