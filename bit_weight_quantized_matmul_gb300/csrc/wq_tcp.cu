@@ -210,12 +210,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   constexpr int NISSUE = FOLD ? 4 : 1;  // MMA issuers; fold mode: two per chunk
   constexpr int CHUNK_COMMITS = FOLD ? 2 : 1;
   constexpr int SUB = S::SUB;
-  // Fold mode: each dequant warp decodes whole chunks and the kDeqQ warps of a TMEM lane quarter
-  // take alternate chunks, so one warp's TMEM stores drain while the other decodes; the other
-  // modes split every chunk among the quarter's warps.
-  constexpr bool ALT = FOLD;
-  constexpr int DEQ_PER_CHUNK = ALT ? 4 : kDeqWarps;  // dequant warps that arrive for one chunk
-  constexpr int NE = ALT ? KC : KC / kDeqQ;  // elements of a row each dequant warp decodes per chunk
+  constexpr int NE = KC / kDeqQ;  // elements of a row each dequant warp decodes per chunk
   static_assert(NE == 32 || NE % 64 == 0, "a dequant warp decodes half a 64-block or whole blocks");
   constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
   constexpr int WCHUNK = Fmt<FMT>::WB * SUB;  // packed bytes of one row per chunk
@@ -251,9 +246,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&xfull[i], 1);
-      mbar_init(&empty[i], CHUNK_COMMITS + DEQ_PER_CHUNK);
+      mbar_init(&empty[i], CHUNK_COMMITS + kDeqWarps);
     }
-    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], DEQ_PER_CHUNK); mbar_init(&aempty[i], CHUNK_COMMITS); }
+    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], CHUNK_COMMITS); }
     mbar_init(done, NWARPS);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&dfull[i], 1);   // kScaleFold: a partial-tile slot is full
@@ -394,7 +389,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------ dequant warps: half h of every chunk
     const int q = warp & 3;
-    const int h = (warp - 2) / 4;  // which 1/kDeqQ of the chunk (ALT: which chunks, g % kDeqQ)
+    const int h = (warp - 2) / 4;  // which 1/kDeqQ of the chunk
     const int r = q * 32 + lane;
     const int lsel = (LUTREP > 1) ? (lane & (LUTREP - 1)) : 0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -414,14 +409,13 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       const int64_t g0 = ((int64_t)ic.nt * kRows * nb) / 256;  // NF4: first s2 group of the tile
       const float off = (FMT == WQ_NF4 && !FOLD) ? s2s[kS2Max - 1] : 0.0f;
       for (int c = 0; c < nch; ++c, ++g) {
-        if (ALT && g % kDeqQ != h) continue;
         const int s = g % STAGES, slot = g % kNA;
         constexpr int NBW = (NE >= 64) ? NE / 64 : 1;  // 64-blocks (or half of one) this warp decodes
         uint32_t sword[NBW];
 #pragma unroll
         for (int bb = 0; bb < NBW; ++bb) {
           // the 64-block this warp decodes (NE >= 64), or the block holding its half (NE == 32)
-          const int blk = (NE >= 64) ? (KC / 64) * c + (ALT ? 0 : NBW * h) + bb : (KC / 64) * c + h / 2;
+          const int blk = (NE >= 64) ? (KC / 64) * c + NBW * h + bb : (KC / 64) * c + h / 2;
           sword[bb] = 0u;
           if (!FOLD && row_ok && blk < nb) {
             if (FMT == WQ_NF4) {
@@ -438,7 +432,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         const uint8_t* wstage = smem + S::W_OFF + s * S::WB;
         constexpr int NES = NE / NBW;                          // elements per decode call (32 or 64)
         constexpr int CPS = NES / (FMT == WQ_Q8_0 ? 16 : 32);  // 16-byte chunks per call
-        const int ck0 = ALT ? 0 : h * (WCHUNK / (16 * kDeqQ));  // first 16-byte chunk of this warp's part
+        const int ck0 = h * (WCHUNK / (16 * kDeqQ));            // first 16-byte chunk of this warp's part
 #pragma unroll
         for (int bb = 0; bb < NBW; ++bb) {
           uint32_t v[NES / 2];
@@ -452,7 +446,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
             decode_span<FMT, NES, LUTREP>(sword[bb], part, wv, lut, lsel, v);
           else
             decode_span_bf16<FMT, NES, LUTREP, MODE == kScaleBF16>(sword[bb], part, wv, lut32, lsel, v);
-          tmem_st_n(tmem_base + lane_base + slot * T::ACOLS + (ALT ? 0 : h * (NE / 2)) + bb * (NES / 2), v);
+          tmem_st_n(tmem_base + lane_base + slot * T::ACOLS + h * (NE / 2) + bb * (NES / 2), v);
         }
         tc_wait_st();
         tc_fence_before();
