@@ -135,7 +135,9 @@ int wq_quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_i
  * M == 0 is a no-op.  Dispatch: M <= 16 runs the decode path (tensor-core
  * GEMV, split-K over a thread-block cluster); larger M runs the persistent
  * tensor-core GEMM; K not a multiple of 64 runs a CUDA-core kernel with the
- * same per-weight decode.                                                       */
+ * same per-weight decode.  WQ_NVFP4_W4A4 with M > 16 and K a multiple of 256
+ * runs the block-scaled FP4 tensor-core GEMM (both operands packed); other
+ * W4A4 shapes run the CUDA-core kernel.                                         */
 int wq_linear(const void* x, const void* packed, const void* scales, int fmt,
               int64_t M, int64_t N, int64_t K, const uint16_t* bias, void* y, void* stream);
 
