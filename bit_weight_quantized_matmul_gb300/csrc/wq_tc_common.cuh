@@ -127,50 +127,6 @@ __device__ __forceinline__ uint32_t scale_word(const uint8_t* __restrict__ scale
   return *reinterpret_cast<const uint32_t*>(scales + n * (K / 16) + 4 * c);
 }
 
-// Decode half h (elements [32h, 32h + 32)) of one 64-element chunk of a weight row
-// into 16 bf16x2 words.  `wrow` points at the row's packed chunk in shared memory.
-template <int FMT>
-__device__ __forceinline__ void decode_half(uint32_t sword, const uint8_t* wrow, const float2* lut, int h,
-                                            uint32_t (&out)[16]) {
-  if (FMT == WQ_Q8_0) {
-    const float d = f16_bits_to_f32(h ? (sword >> 16) : (sword & 0xFFFFu));
-    const uint4* src = reinterpret_cast<const uint4*>(wrow + 32 * h);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint4 v = src[q];
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a0 = (float)(int8_t)(u[j] & 0xFF), a1 = (float)(int8_t)((u[j] >> 8) & 0xFF);
-        const float a2 = (float)(int8_t)((u[j] >> 16) & 0xFF), a3 = (float)(int8_t)(u[j] >> 24);
-        out[q * 8 + j * 2] = pack_bf16x2(__fmul_rn(a0, d), __fmul_rn(a1, d));
-        out[q * 8 + j * 2 + 1] = pack_bf16x2(__fmul_rn(a2, d), __fmul_rn(a3, d));
-      }
-    }
-    return;
-  }
-  float sc0, sc1;  // scale of elements [0, 16) and [16, 32) of this half
-  if (FMT == WQ_NF4) {
-    sc0 = sc1 = __uint_as_float(sword);
-  } else if (FMT == WQ_Q4_0) {
-    sc0 = sc1 = f16_bits_to_f32(h ? (sword >> 16) : (sword & 0xFFFFu));
-  } else {
-    sc0 = e4m3_to_f32((sword >> (16 * h)) & 0xFFu);
-    sc1 = e4m3_to_f32((sword >> (16 * h + 8)) & 0xFFu);
-  }
-  const uint4 v = *reinterpret_cast<const uint4*>(wrow + 16 * h);
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float s = (j < 2) ? sc0 : sc1;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float2 lv = lut[(u[j] >> (8 * b)) & 0xFFu];
-      out[j * 4 + b] = pack_bf16x2(__fmul_rn(lv.x, s), __fmul_rn(lv.y, s));
-    }
-  }
-}
-
 // Decode NE (32 or 64) consecutive weights of one 64-element block of a row into NE/2
 // bf16x2 words.  `part` selects which NE-element part of the block (0 when NE == 64);
 // `sword` is the block's scale word (see scale_word); `wv` holds the NE packed codes
