@@ -3,11 +3,17 @@
 Headline workload (one "step"): the 40 decoder Linears of a whisper-large-v3-turbo-shaped
 model (4 layers x {self q,k,v,o; cross q,k,v,o; fc1 1280->5120; fc2 5120->1280}), NF4 with
 double-quantised absmax, bf16 activations, one pass at each of M = 1, 4 and 16 rows:
-120 fused dequant-matmuls, run as one grouped launch per M (the 40 Linears of the sweep
-have independent inputs, so one persistent kernel streams all their weights).  Weights are packed once (load time) and stay resident;
-every step reads a different weight copy (9 copies, 487 MB > 3x the 129 MB L2), so each
-step streams its weights from HBM.  Metric: algorithmic GB/s (packed weights + scales + x +
-y + bias bytes per step / device time).
+120 fused dequant-matmuls, run as one grouped launch per M (the 40 Linears of one pass have
+independent inputs, so one persistent kernel streams all their weights).  Weights are packed
+once (load time) and stay resident; every step reads a different weight copy (9 copies,
+487 MB > 3x the 129 MB L2), so each step streams its weights from HBM.  Metric: algorithmic
+GB/s (packed weights + scales + x + y + bias bytes per step / device time).
+
+Beside the headline the JSON line carries the shapes a real decode step runs (each Linear as
+its own dependent launch: `chained`, `per_linear`), a per-replay distribution (median / p10 /
+p90), a clock-sampled window, the end-to-end number through the public API with host buffers,
+the encoder GEMM lines (W4A16, W4A4 with and without the activation quantiser, the config-2 /
+config-3 sweeps), the q4_0 / q8_0 232-Linear sweep, and the CPU oracle on the host cores.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
 
@@ -17,6 +23,7 @@ N > 1 runs one process per GPU (torchrun), each an independent replica of the wo
 workload.
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -32,6 +39,15 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# dense FP4 over dense bf16 tensor throughput, nominal GB300 figures (13.5 / 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0
+L2_FLUSH_BYTES = 256 * 1024 * 1024
+
+# the kernel sources a DRAM-traffic capture depends on (a capture is stale once these change)
+CSRC = os.path.join(ROOT, "bit_weight_quantized_matmul_gb300", "csrc")
+KERNEL_SOURCES = {
+    "decoder_nf4": ["wq_tcp.cu", "wq_tc_common.cuh", "wq_device.cuh"],
+}
 
 
 # ---------------------------------------------------------------- helpers
@@ -84,21 +100,52 @@ def peak_tflops(peaks, sustained):
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def pct(vals, q):
+    """q-th percentile (0..100) of a list, linear interpolation."""
+    return float(np.percentile(np.asarray(vals, np.float64), q))
+
+
+def source_hash(workload):
+    """sha256 (first 16 hex digits) of the kernel sources a DRAM-traffic capture depends on."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES.get(workload, []):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, only when the kernel sources it was
+    captured from are unchanged (else None and a note)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f).get(workload, {})
+    except Exception:
+        return None, "no capture"
+    if not d.get("source_sha16"):
+        return None, "capture has no source hash"
+    if d["source_sha16"] != source_hash(workload):
+        return None, "stale: kernel sources changed since the capture"
+    return d.get("dram_bytes_per_launch"), "captured on the current kernel sources"
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    """nvidia-smi clock / throttle-reason samples of one GPU (selected by UUID) while it runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
+    def __init__(self, gpu_id, period_ms=100):
+        self.gpu = gpu_id
+        self.period = period_ms
         self.proc = None
         self.lines = []
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -111,13 +158,13 @@ class ClockSampler:
 
     def stop(self):
         if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -126,6 +173,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for nm, v in zip(names, parts[5:9]):
@@ -133,12 +181,48 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(local_rank):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return local_rank
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
 
 
 # ---------------------------------------------------------------- workload
 def nf4_linear_bytes(N, K, M, has_bias):
     w = N * K // 2 + N * K // 64 + 4 * ((N * K // 64 + 255) // 256) + 4
+    return w + M * K * 2 + M * N * 2 + (N * 2 if has_bias else 0)
+
+
+def linear_bytes(fmt, N, K, M, has_bias):
+    """Algorithmic bytes of one Linear call: packed weight + scales + x + y + bias."""
+    if fmt == "nf4":
+        return nf4_linear_bytes(N, K, M, has_bias)
+    if fmt in ("nvfp4", "nvfp4_w4a4"):
+        w = N * K // 2 + N * K // 16 + 4
+    elif fmt == "q4_0":
+        w = N * K // 2 + N * K // 32 * 2
+    elif fmt == "q8_0":
+        w = N * K + N * K // 32 * 2
+    else:
+        raise ValueError(fmt)
     return w + M * K * 2 + M * N * 2 + (N * 2 if has_bias else 0)
 
 
@@ -151,10 +235,76 @@ def step_bytes(linears, Ms):
     return sum(nf4_linear_bytes(l["N"], l["K"], M, l["bias"]) for M in Ms for l in linears)
 
 
+def carve(torch, shapes, dev, dtype=None):
+    """One contiguous bf16 buffer holding every [m, n] matrix of `shapes` (views, each 16-byte
+    aligned), so a step's activations or outputs move in one copy each way."""
+    dtype = dtype or torch.bfloat16
+    sizes = [(m * n + 7) // 8 * 8 for m, n in shapes]
+    flat = torch.empty(sum(sizes), dtype=dtype, device=dev)
+    views, off = [], 0
+    for (m, n), sz in zip(shapes, sizes):
+        views.append(flat[off:off + m * n].view(m, n))
+        off += sz
+    return flat, views
+
+
+# ---------------------------------------------------------------- timing
+class Timer:
+    """CUDA-event timing on one stream; every region is bracketed by synchronisation (and a
+    barrier over ranks)."""
+
+    def __init__(self, torch, stream, world, dev):
+        self.torch, self.stream, self.world, self.dev = torch, stream, world, dev
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def region(self, fn, n):
+        """Device time (ms, max over ranks) of fn(k) for k in range(n), recorded on the stream."""
+        torch = self.torch
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(self.stream):
+            ev0.record(self.stream)
+            for k in range(n):
+                fn(k)
+            ev1.record(self.stream)
+        torch.cuda.synchronize()
+        self.barrier()
+        return max_over_ranks(ev0.elapsed_time(ev1), self.world, self.dev)
+
+    def each(self, fn, n, before=None):
+        """Per-call device times (ms) of fn(k), each bracketed by its own events; `before(k)`
+        runs between calls outside the events (e.g. an L2 flush)."""
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(self.stream):
+            for k in range(n):
+                if before is not None:
+                    before(k)
+                evs[k][0].record(self.stream)
+                fn(k)
+                evs[k][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+
+def dist_summary(ms_list, bytes_or_flops, unit):
+    """median / p10 / p90 of per-rep times and the matching throughputs."""
+    scale = 1e9 if unit == "GB/s" else 1e12
+    med, p10, p90 = pct(ms_list, 50), pct(ms_list, 10), pct(ms_list, 90)
+    thr = lambda t: round(bytes_or_flops / (t * 1e-3) / scale, 2)
+    return {"reps": len(ms_list), "ms_median": round(med, 5), "ms_p10": round(p10, 5), "ms_p90": round(p90, 5),
+            "value_median": thr(med), "value_p10_time": thr(p10), "value_p90_time": thr(p90), "unit": unit}
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, local_rank, world):
     import torch
-    import torch.distributed as dist
     from bit_weight_quantized_matmul_gb300 import build as B
     B.build()
     from bit_weight_quantized_matmul_gb300 import wq
@@ -164,7 +314,6 @@ def run_ours(args, rank, local_rank, world):
     dev = torch.device("cuda", local_rank)
     linears, Ms = decoder_workload()
     R = 9  # weight copies: 9 x 54 MB > 3 x L2
-    # pack once from the seeded generator, then clone to R resident copies
     packed0 = []
     for l in linears:
         W = torch.from_numpy(wl.weight(l["seed"], l["N"], l["K"])).to(dev)
@@ -172,18 +321,8 @@ def run_ours(args, rank, local_rank, world):
         del W
     copies = [packed0] + [[(p.clone(), s.clone()) for p, s in packed0] for _ in range(R - 1)]
     biases = [wl.bias(l["seed"], l["N"]).to(dev) if l["bias"] else None for l in linears]
-    # every activation / output of a step lives in one contiguous buffer (views per Linear, each
-    # 16-byte aligned), so the end-to-end run moves a step's inputs and results in one copy each way
-    def carve(shapes, fill=None):
-        sizes = [(m * n + 7) // 8 * 8 for m, n in shapes]
-        flat = torch.empty(sum(sizes), dtype=torch.bfloat16, device=dev)
-        views, off = [], 0
-        for (m, n), sz in zip(shapes, sizes):
-            views.append(flat[off:off + m * n].view(m, n))
-            off += sz
-        return flat, views
-    x_flat, x_views = carve([(M, l["K"]) for M in Ms for l in linears])
-    y_flat, y_views = carve([(M, l["N"]) for M in Ms for l in linears])
+    x_flat, x_views = carve(torch, [(M, l["K"]) for M in Ms for l in linears], dev)
+    y_flat, y_views = carve(torch, [(M, l["N"]) for M in Ms for l in linears], dev)
     xs = {M: x_views[j * len(linears):(j + 1) * len(linears)] for j, M in enumerate(Ms)}
     ys = {M: y_views[j * len(linears):(j + 1) * len(linears)] for j, M in enumerate(Ms)}
     for M in Ms:
@@ -192,6 +331,7 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
+    T = Timer(torch, stream, world, dev)
 
     def grouped_pass(copy, M):
         probs = [(ys[M][i], xs[M][i], copies[copy][i][0], copies[copy][i][1], l["N"], l["K"], biases[i])
@@ -203,8 +343,7 @@ def run_ours(args, rank, local_rank, world):
             p, s = copies[copy][i]
             wq.linear_into(ys[M][i], xs[M][i], p, s, "nf4", l["N"], l["K"], biases[i], weights_static=True)
 
-    # eager warm-up of every path once (sets kernel attributes before capture)
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):  # eager warm-up of every path (sets kernel attributes before capture)
         for M in Ms:
             grouped_pass(0, M)
             chained_pass(0, M)
@@ -225,47 +364,46 @@ def run_ours(args, rank, local_rank, world):
     launches_per_step = len(Ms)
     bytes_per_step = step_bytes(linears, Ms)
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def timed(gs, steps):
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for k in range(steps):
-                gs[k % 3].replay()
-            ev1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        return max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-
     with torch.cuda.stream(stream):
         for w in range(args.warmup):
             graphs[w % 3].replay()
             chained_graphs[w % 3].replay()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(gpu_uuid(local_rank))
     clocks.start()
-    t_ms = timed(graphs, args.steps)
+    # ---- the contract's timed region: exactly K steps
+    t_ms = T.region(lambda k: graphs[k % 3].replay(), args.steps)
+    # ---- a clock-sampled window of the same replays (>= args.clock_seconds of device time), so the
+    # clock record has samples even when K steps last a millisecond
+    win_steps, win_ms = 0, 0.0
+    batch = max(100, int(0.2 / max(t_ms / args.steps * 1e-3, 1e-6)))
+    while win_ms < 1000 * args.clock_seconds:
+        win_ms += T.region(lambda k: graphs[k % 3].replay(), batch)
+        win_steps += batch
     clk = clocks.stop()
     ms_per_step = t_ms / args.steps
     value = job_throughput(bytes_per_step, args.steps, world, t_ms * 1e-3)  # GB/s, all ranks
+    reps = T.each(lambda k: graphs[k % 3].replay(), args.reps)
+    per_rep = dist_summary(reps, bytes_per_step, "GB/s")
+    window = {"steps": win_steps, "seconds": round(win_ms / 1000, 3),
+              "value": round(bytes_per_step * win_steps / (win_ms * 1e-3) / 1e9, 2), "unit": "GB/s"}
+    sm = clk.get("sm_mhz")
+    if sm:
+        clk["time_x_median_mhz"] = round(ms_per_step * sm, 3)
+
     ch_steps = max(3, min(args.steps, 2000))
-    t_ch = timed(chained_graphs, ch_steps)
+    t_ch = T.region(lambda k: chained_graphs[k % 3].replay(), ch_steps)
     chained = {"value": round(bytes_per_step * ch_steps / (t_ch * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "ms_per_step": round(t_ch / ch_steps, 5), "steps": ch_steps,
-               "what": "same step as 120 dependent single-Linear launches (split-K cluster kernel), "
-                       "CUDA graph with programmatic dependent launch"}
+               "ms_per_step": round(t_ch / ch_steps, 5), "us_per_linear": round(1000 * t_ch / ch_steps / 120, 3),
+               "steps": ch_steps,
+               "what": "same step as 120 dependent single-Linear launches (wq_linear each), CUDA graph with "
+                       "programmatic dependent launch"}
 
     # ---- end to end through the public API: pinned host x in, y out, every step
     xh = x_flat.cpu().pin_memory()
     yh = torch.empty(y_flat.shape, dtype=y_flat.dtype).pin_memory()
-    h2d = x_flat.numel() * 2
-    d2h = y_flat.numel() * 2
+    h2d, d2h = x_flat.numel() * 2, y_flat.numel() * 2
     e2e_steps = max(3, min(args.steps, 200))
 
     def e2e_step(k):
@@ -277,7 +415,7 @@ def run_ours(args, rank, local_rank, world):
 
     for k in range(2):
         e2e_step(k)
-    barrier()
+    T.barrier()
     t0 = time.perf_counter()
     for k in range(e2e_steps):
         e2e_step(k)
@@ -287,7 +425,7 @@ def run_ours(args, rank, local_rank, world):
     peaks = read_peaks()
     pk, pk_src = peak_hbm(peaks)
     achieved = bytes_per_step / (ms_per_step * 1e-3) / 1e9  # per GPU; same kernel throughout the region
-    traffic = load_traffic("wq_tcp_kernel", "decoder_nf4")
+    traffic, traffic_note = load_traffic("decoder_nf4")
     out = {
         "metric": "4-bit dequant-linear effective HBM bandwidth, decode (M<=16)",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -295,7 +433,7 @@ def run_ours(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "nf4 weights, bf16 activations, fp32 accumulate",
         "data": "synthetic (seeded counter-based generator; random-init weights of the model's shapes)",
         "config": {"workload": "whisper-large-v3-turbo decoder sweep: 4 layers x 10 NF4 Linears "
-                               "(1280x1280 x8, 5120x1280, 1280x5120), M in {1,4,16} -> 120 launches/step",
+                               "(1280x1280 x8, 5120x1280, 1280x5120), M in {1,4,16} -> 120 Linear-calls/step",
                    "fmt": "nf4 block 64, double-quant absmax (int8 per 256, fp32 scale)",
                    "l2": "inputs larger than L2: 9 rotated weight copies (487 MB)",
                    "bytes_per_step": bytes_per_step,
@@ -303,10 +441,12 @@ def run_ours(args, rank, local_rank, world):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk, "unit": "GB/s",
                      "frac": round(achieved / pk, 4), "peak_source": pk_src, "traffic": traffic,
-                     "kernel": "wq_tcp_kernel (persistent grouped decode: BN=16, 256-element chunks, "
-                               "block scales folded after the MMA)",
+                     "traffic_note": traffic_note, "kernel_source_sha16": source_hash("decoder_nf4"),
+                     "kernel": "wq_tcp_kernel (persistent grouped decode, BN=16)",
                      "algorithmic_bytes_per_launch": round(bytes_per_step / launches_per_step, 1)},
         "clocks": clk,
+        "clock_window": window,
+        "per_rep": per_rep,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "note": "per step: one pinned-host -> device copy of all 120 activations, the 3 grouped "
@@ -314,82 +454,254 @@ def run_ours(args, rank, local_rank, world):
         "chained": chained,
         "gpu_launches": launches_per_step * args.steps,
     }
+    if rank == 0 and not args.no_extra:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        out["per_linear"] = per_linear(torch, wq, T, flush, linears, copies, xs, ys, biases, Ms)
+        del copies, packed0
+        torch.cuda.empty_cache()
+        out["extra"] = extra_lines(args, torch, wq, wl, dev, T, flush, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
-    if rank == 0 and not args.no_extra:
-        out["extra"] = extra_gemm(wq, wl, dev, peaks)
+        out["cpu_baseline"]["one_core"] = cpu_baseline_one_core(args.cpu_seconds_one_core)
     return out
 
 
-def load_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, when it matches the current kernel."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    try:
-        with open(path) as f:
-            d = json.load(f)
-        return d.get(workload, {}).get("dram_bytes_per_launch")
-    except Exception:
-        return None
+def per_linear(torch, wq, T, flush, linears, copies, xs, ys, biases, Ms):
+    """Each decoder Linear shape alone, as a real decode step runs it: one wq_linear call per Linear.
+    back_to_back: every stored copy of that shape (all distinct weights, > L2 in total for the
+    1280 x 1280 shape) as dependent launches in one CUDA graph with programmatic dependent launch;
+    isolated: one launch after an L2 flush, median of 30."""
+    res = {}
+    shapes = {"1280x1280": lambda l: l["N"] == 1280 and l["K"] == 1280,
+              "fc1_5120x1280": lambda l: l["N"] == 5120,
+              "fc2_1280x5120": lambda l: l["K"] == 5120}
+    for name, sel in shapes.items():
+        idx = [i for i, l in enumerate(linears) if sel(l)]
+        N, K = linears[idx[0]]["N"], linears[idx[0]]["K"]
+        for M in Ms:
+            calls = [(c, i) for c in range(len(copies)) for i in idx]
+
+            def launch(c, i):
+                p, s = copies[c][i]
+                wq.linear_into(ys[M][i], xs[M][i], p, s, "nf4", N, K, biases[i], weights_static=True)
+
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(T.stream):
+                launch(*calls[0])
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=T.stream):
+                for c, i in calls:
+                    launch(c, i)
+            t_bb = T.region(lambda k: g.replay(), 3) / 3 / len(calls)
+            iso = T.each(lambda k: launch(*calls[k % len(calls)]), 30, before=lambda k: flush.zero_())
+            nb = nf4_linear_bytes(N, K, M, True)
+            res[f"{name}_M{M}"] = {
+                "back_to_back_us": round(1000 * t_bb, 3), "back_to_back_GBps": round(nb / (t_bb * 1e-3) / 1e9, 1),
+                "isolated_us_median": round(1000 * pct(iso, 50), 3),
+                "isolated_GBps": round(nb / (pct(iso, 50) * 1e-3) / 1e9, 1), "launches": len(calls)}
+            del g
+    return res
 
 
-def extra_gemm(wq, wl, dev, peaks):
-    """Encoder-side context (configs 2 and 3 shapes): the fc1 Linear (N=5120, K=1280) at
-    M = 1500 x 4 in NVFP4 W4A16, and in W4A4 (GEMM alone, and with the runtime activation
-    quantiser); each measured call is one CUDA graph (the quantiser's kernels and the GEMM
-    replay back to back); L2 flushed before every replay; median of 10."""
-    import torch
+def extra_lines(args, torch, wq, wl, dev, T, flush, peaks):
+    """Encoder-side and sweep lines, each launch (or CUDA-graph replay) timed with CUDA events
+    after an L2 flush outside the events; median over reps."""
+    pk, src = peak_tflops(peaks, sustained=False)
+    hbm, _ = peak_hbm(peaks)
+    fp4 = FP4_OVER_BF16 * pk
+    out = {"peak": {"bf16_tflops": pk, "source": src,
+                    "fp4_tflops": fp4, "fp4_source": f"{src} bf16 x {FP4_OVER_BF16:g} (nominal dense FP4 / bf16 ratio)",
+                    "hbm_gbs": hbm}}
+
+    def graph_of(fn):
+        with torch.cuda.stream(T.stream):
+            for _ in range(2):
+                fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=T.stream):
+            fn()
+        return g
+
+    def med_ms(g, reps=10):
+        return pct(T.each(lambda k: g.replay(), reps, before=lambda k: flush.zero_()), 50)
+
+    # ---- encoder fc1 at M = 6000 (4 x 1500 frames), NVFP4
     M, N, K = 6000, 5120, 1280
     W = torch.from_numpy(wl.weight(101, N, K)).to(dev)
     p, s = wq.pack("nvfp4", W)
+    del W
     x = wl.activations(101, M, K, outlier_frac=0.001).to(dev)
     b = wl.bias(101, N).to(dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     act = (torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
            torch.empty((M, K // 16), dtype=torch.uint8, device=dev),
            torch.empty(1, dtype=torch.float32, device=dev))
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    g_static = torch.tensor([float(np.abs(wl.bf16_as_f32(x.cpu())).max()) / 2688.0], dtype=torch.float32,
+                            device=dev)
+    fl = 2.0 * M * N * K
+    tf = lambda t: round(fl / (t * 1e-3) / 1e12, 1)
+    # W4A4 bytes: W codes + scales, x codes + scales, y bf16, bias
+    w4_bytes = N * K // 2 + N * K // 16 + M * K // 2 + M * K // 16 + 2 * M * N + 2 * N
+    attain = min(fp4, hbm * fl / w4_bytes / 1e3)  # TFLOP/s: min(FP4 peak, HBM x arithmetic intensity)
+    t16 = med_ms(graph_of(lambda: wq.linear_into(y, x, p, s, "nvfp4", N, K, b)))
+    wq.quant_act_nvfp4(x, out=act)
+    t44 = med_ms(graph_of(lambda: wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b)))
+    t44q = med_ms(graph_of(lambda: (wq.quant_act_nvfp4(x, out=act),
+                                    wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b))))
+    t44s = med_ms(graph_of(lambda: (wq.quant_act_nvfp4(x, g_in=g_static, out=act),
+                                    wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b))))
+    out["encoder_fc1_M6000"] = {
+        "workload": "encoder fc1 (N=5120, K=1280) at M=6000 (4 x 1500 frames), NVFP4 weights, L2 flushed",
+        "w4a16": {"value": tf(t16), "unit": "TFLOP/s", "ms": round(t16, 4), "frac_of_bf16_peak": round(tf(t16) / pk, 4)},
+        "w4a4_gemm": {"value": tf(t44), "unit": "TFLOP/s", "ms": round(t44, 4),
+                      "frac_of_fp4_peak": round(tf(t44) / fp4, 4),
+                      "attainable_tflops": round(attain, 1), "frac_of_attainable": round(tf(t44) / attain, 4),
+                      "attainable_note": "min(FP4 peak, HBM peak x FLOP per algorithmic byte)"},
+        "w4a4_with_act_quant_dynamic_g": {"value": tf(t44q), "unit": "TFLOP/s", "ms": round(t44q, 4)},
+        "w4a4_with_act_quant_static_g": {"value": tf(t44s), "unit": "TFLOP/s", "ms": round(t44s, 4)},
+    }
+    del p, s, x, y, act, b
+    torch.cuda.empty_cache()
 
-    def timed(fn):
-        for _ in range(3):
+    out["encoder_sweeps"] = encoder_sweeps(torch, wq, wl, dev, T, flush, pk, fp4)
+    out["c4_sweep"] = c4_sweep(torch, wq, wl, dev, T, flush, pk, hbm)
+    return out
+
+
+def encoder_sweeps(torch, wq, wl, dev, T, flush, pk, fp4, steps=3):
+    """Configs 2 and 3: the encoder Linear shapes (q/k/v/o 1280x1280, fc1 5120x1280, fc2 1280x5120) at
+    M = 1500 x B, B in {1, 4, 16}: 9 GEMMs per step, NVFP4 weights, activations with 0.1 % outliers x20;
+    W4A16, and W4A4 with the dynamic activation quantiser inside each GEMM's graph."""
+    cases = []
+    for si, (name, N, K) in enumerate(wl.encoder_shapes()):
+        W = torch.from_numpy(wl.weight(100 + si, N, K)).to(dev)
+        p, s = wq.pack("nvfp4", W)
+        del W
+        b = wl.bias(100 + si, N).to(dev)
+        for Bw in (1, 4, 16):
+            M = 1500 * Bw
+            x = wl.activations(100 + si, M, K, outlier_frac=0.001).to(dev)
+            cases.append(dict(name=name, B=Bw, M=M, N=N, K=K, p=p, s=s, b=b, x=x,
+                              y=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                              act=(torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                                   torch.empty((M, K // 16), dtype=torch.uint8, device=dev),
+                                   torch.empty(1, dtype=torch.float32, device=dev))))
+    res = {}
+    for mode in ("w4a16", "w4a4"):
+        def launch(c):
+            if mode == "w4a4":
+                wq.quant_act_nvfp4(c["x"], out=c["act"])
+                wq.linear_into(c["y"], c["act"], c["p"], c["s"], "nvfp4_w4a4", c["N"], c["K"], c["b"])
+            else:
+                wq.linear_into(c["y"], c["x"], c["p"], c["s"], "nvfp4", c["N"], c["K"], c["b"])
+        graphs = []
+        for c in cases:
+            with torch.cuda.stream(T.stream):
+                launch(c)
+                launch(c)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=T.stream):
+                launch(c)
+            graphs.append(g)
+        per = T.each(lambda k: graphs[k % len(cases)].replay(), steps * len(cases), before=lambda k: flush.zero_())
+        flops = sum(2.0 * c["M"] * c["N"] * c["K"] for c in cases)
+        value = flops * steps / (sum(per) * 1e-3) / 1e12
+        peak = fp4 if mode == "w4a4" else pk
+        by = {}
+        for i, c in enumerate(cases):
+            ts = [per[j] for j in range(i, len(per), len(cases))]
+            by[f"{c['name']}_B{c['B']}"] = round(2.0 * c["M"] * c["N"] * c["K"] / (pct(ts, 50) * 1e-3) / 1e12, 1)
+        res[mode] = {"value": round(value, 1), "unit": "TFLOP/s", "frac_of_peak": round(value / peak, 4),
+                     "peak": peak, "per_gemm_tflops_median": by, "steps": steps,
+                     "what": ("config 3: W4A4, dynamic activation quantiser in each GEMM's graph" if mode == "w4a4"
+                              else "config 2: W4A16")}
+        del graphs
+    return res
+
+
+def c4_sweep(torch, wq, wl, dev, T, flush, pk, hbm, steps=3):
+    """Config 4: the 232 Linears of the large-v3-turbo shape in model order, q8_0 for the 32 encoder
+    layers (192 GEMMs at M = 1500) and q4_0 for the 4 decoder layers (40 Linears at M = 1).  Weights
+    for this throughput line come from torch's seeded normal generator on the GPU (N(0, 0.02^2), one
+    seed per Linear from the splitmix64 chain): the same shapes and distribution as the parity tests'
+    counter-based generator, without generating 735 M values on the host."""
+    sweep = wl.turbo_full_sweep()
+    enc = [l for l in sweep if l["part"] == "encoder"]
+    dec = [l for l in sweep if l["part"] == "decoder"]
+    gen = torch.Generator(device=dev)
+
+    def packed(l, fmt):
+        gen.manual_seed(l["seed"] % (1 << 63))
+        W = torch.randn((l["N"], l["K"]), generator=gen, device=dev, dtype=torch.float32) * 0.02
+        return wq.pack(fmt, W)
+
+    res = {}
+    # decoder: q4_0, M = 1, the 40 Linears as one grouped launch (independent inputs) and as 40
+    # dependent launches
+    dw = [packed(l, "q4_0") for l in dec]
+    db = [wl.bias(l["seed"] % (1 << 31), l["N"]).to(dev) if l["bias"] else None for l in dec]
+    dx = [torch.randn((1, l["K"]), generator=gen, device=dev).to(torch.bfloat16) for l in dec]
+    dy = [torch.empty((1, l["N"]), dtype=torch.bfloat16, device=dev) for l in dec]
+    nbytes = sum(linear_bytes("q4_0", l["N"], l["K"], 1, l["bias"]) for l in dec)
+
+    def grouped():
+        wq.linear_grouped([(dy[i], dx[i], dw[i][0], dw[i][1], l["N"], l["K"], db[i]) for i, l in enumerate(dec)],
+                          "q4_0", weights_static=True)
+
+    def chained():
+        for i, l in enumerate(dec):
+            wq.linear_into(dy[i], dx[i], dw[i][0], dw[i][1], "q4_0", l["N"], l["K"], db[i], weights_static=True)
+
+    for nm, fn in (("decoder_q4_0_grouped", grouped), ("decoder_q4_0_chained", chained)):
+        with torch.cuda.stream(T.stream):
             fn()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+        with torch.cuda.graph(g, stream=T.stream):
             fn()
-        ts = []
-        for _ in range(10):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            g.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+        ts = T.each(lambda k: g.replay(), 10, before=lambda k: flush.zero_())
+        res[nm] = {"value": round(nbytes / (pct(ts, 50) * 1e-3) / 1e9, 1), "unit": "GB/s",
+                   "us": round(1000 * pct(ts, 50), 2), "frac_of_hbm": round(nbytes / (pct(ts, 50) * 1e-3) / 1e9 / hbm, 4),
+                   "bytes": nbytes, "note": "L2 flushed before each replay; 40 Linears at M = 1"}
+        del g
+    del dw, dx, dy, db
+    torch.cuda.empty_cache()
+    # encoder: q8_0, M = 1500, 192 GEMMs in model order, one CUDA graph per step
+    ew = [packed(l, "q8_0") for l in enc]
+    eb = {}
+    ex = {K: torch.randn((1500, K), generator=gen, device=dev).to(torch.bfloat16) for K in (1280, 5120)}
+    ey = {N: torch.empty((1500, N), dtype=torch.bfloat16, device=dev) for N in (1280, 5120)}
+    for l in enc:
+        if l["bias"]:
+            eb[l["seed"]] = torch.randn(l["N"], generator=gen, device=dev).mul_(0.01).to(torch.bfloat16)
 
-    t16 = timed(lambda: wq.linear_into(y, x, p, s, "nvfp4", N, K, b))
-    wq.quant_act_nvfp4(x, out=act)
-    t44 = timed(lambda: wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b))
-    t44q = timed(lambda: (wq.quant_act_nvfp4(x, out=act), wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b)))
-    fl = 2.0 * M * N * K
-    pk, src = peak_tflops(peaks, sustained=False)
-    tf = lambda t: round(fl / (t * 1e-3) / 1e12, 1)
-    return {"workload": "encoder fc1 (N=5120, K=1280) at M=6000 (4 x 1500 frames), L2 flushed",
-            "w4a16_nvfp4": {"value": tf(t16), "unit": "TFLOP/s", "ms": round(t16, 4),
-                            "frac_of_bf16_peak": round(tf(t16) / pk, 4)},
-            "w4a4_nvfp4_gemm": {"value": tf(t44), "unit": "TFLOP/s", "ms": round(t44, 4),
-                                "frac_of_fp4_nominal": round(tf(t44) / (4 * pk), 4)},
-            "w4a4_nvfp4_with_act_quant": {"value": tf(t44q), "unit": "TFLOP/s", "ms": round(t44q, 4)},
-            "peak": {"bf16": pk, "source": src, "fp4": "4 x bf16 (nominal ratio)"}}
+    def enc_step():
+        for i, l in enumerate(enc):
+            wq.linear_into(ey[l["N"]], ex[l["K"]], ew[i][0], ew[i][1], "q8_0", l["N"], l["K"], eb.get(l["seed"]))
+
+    with torch.cuda.stream(T.stream):
+        enc_step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=T.stream):
+        enc_step()
+    ts = T.each(lambda k: g.replay(), steps, before=lambda k: flush.zero_())
+    flops = sum(2.0 * l["M"] * l["N"] * l["K"] for l in enc)
+    v = flops / (pct(ts, 50) * 1e-3) / 1e12
+    res["encoder_q8_0"] = {"value": round(v, 1), "unit": "TFLOP/s", "ms": round(pct(ts, 50), 3),
+                           "frac_of_bf16_peak": round(v / pk, 4), "tflop": round(flops / 1e12, 4),
+                           "note": "192 GEMMs (32 layers x q,k,v,o,fc1,fc2 at M = 1500) in one graph; "
+                                   "activations shared per shape (each GEMM reads its own 1.7-7 MB weight)"}
+    del ew, g
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------- encoder workloads
 def run_encoder(args, rank, local_rank, world):
-    """Configs 2 / 3: the encoder Linear shapes (q/k/v/o 1280x1280, fc1 5120x1280, fc2
-    1280x5120) at M = 1500 x B for B in {1, 4, 16}, NVFP4 weights, bf16 activations with 0.1 %
-    outliers x20; W4A16, or W4A4 with the runtime activation quantiser inside the step.  One step
-    = the 9 GEMMs; each GEMM (with its quantiser, for W4A4) is one CUDA graph replay, timed with
-    CUDA events after an L2 flush (excluded)."""
+    """Configs 2 / 3 as the headline: the 9 encoder GEMMs per step (see encoder_sweeps)."""
     import torch
     from bit_weight_quantized_matmul_gb300 import build as B
     B.build()
@@ -397,74 +709,31 @@ def run_encoder(args, rank, local_rank, world):
     from bit_weight_quantized_matmul_gb300 import workloads as wl
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w4a4 = args.workload == "encoder_w4a4"
-    cases = []
-    for si, (name, N, K) in enumerate(wl.encoder_shapes()):
-        W = torch.from_numpy(wl.weight(100 + si, N, K)).to(dev)
-        p, s = wq.pack("nvfp4", W)
-        b = wl.bias(100 + si, N).to(dev)
-        for Bw in (1, 4, 16):
-            M = 1500 * Bw
-            x = wl.activations(100 + si, M, K, outlier_frac=0.001).to(dev)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            act = (torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
-                   torch.empty((M, K // 16), dtype=torch.uint8, device=dev),
-                   torch.empty(1, dtype=torch.float32, device=dev))
-            cases.append(dict(name=name, B=Bw, M=M, N=N, K=K, p=p, s=s, b=b, x=x, y=y, act=act))
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-
-    def launch(c):
-        if w4a4:
-            wq.quant_act_nvfp4(c["x"], out=c["act"])
-            wq.linear_into(c["y"], c["act"], c["p"], c["s"], "nvfp4_w4a4", c["N"], c["K"], c["b"])
-        else:
-            wq.linear_into(c["y"], c["x"], c["p"], c["s"], "nvfp4", c["N"], c["K"], c["b"])
-
-    for _ in range(args.warmup):
-        for c in cases:
-            launch(c)
-    torch.cuda.synchronize()
-    for c in cases:
-        c["graph"] = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(c["graph"]):
-            launch(c)
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(len(cases) * args.steps)]
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    k = 0
-    for _ in range(args.steps):
-        for c in cases:
-            flush.zero_()
-            ev[k][0].record()
-            c["graph"].replay()
-            ev[k][1].record()
-            k += 1
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    per = [e0.elapsed_time(e1) for e0, e1 in ev]
-    t_ms = max_over_ranks(sum(per), world, dev)
-    flops_step = sum(2.0 * c["M"] * c["N"] * c["K"] for c in cases)
-    value = world * flops_step * args.steps / (t_ms * 1e-3) / 1e12
+    stream = torch.cuda.Stream(device=dev)
+    T = Timer(torch, stream, world, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     peaks = read_peaks()
     pk, src = peak_tflops(peaks, sustained=False)
-    by = {}
-    for i, c in enumerate(cases):
-        ts = sorted(per[j] for j in range(i, len(per), len(cases)))
-        by[f"{c['name']}_B{c['B']}"] = round(2.0 * c["M"] * c["N"] * c["K"] / (ts[len(ts) // 2] * 1e-3) / 1e12, 1)
+    fp4 = FP4_OVER_BF16 * pk
+    clocks = ClockSampler(gpu_uuid(local_rank))
+    clocks.start()
+    sw = encoder_sweeps(torch, wq, wl, dev, T, flush, pk, fp4, steps=args.steps)
+    clk = clocks.stop()
+    w4a4 = args.workload == "encoder_w4a4"
+    r = sw["w4a4" if w4a4 else "w4a16"]
+    value = world * r["value"]
     return {"metric": "4-bit dequant-linear TFLOP/s, encoder (M = 1500 x B)", "value": round(value, 2),
             "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(t_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "nvfp4 weights, " + ("nvfp4 activations" if w4a4 else "bf16 activations"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 weights, " + ("nvfp4 activations" if w4a4 else "bf16 activations"),
             "data": "synthetic (seeded counter-based generator)",
-            "config": {"workload": ("W4A4 (activation quantiser in the step)" if w4a4 else "W4A16") +
-                                   ": encoder Linears qkvo/fc1/fc2 at M=1500*B, B in {1,4,16} (9 GEMMs/step)",
-                       "l2": "flushed (256 MB write) before every launch, outside the timed events",
-                       "launch": "one CUDA graph replay per GEMM (W4A4: the quantiser's kernels and the GEMM)"},
-            "roofline": {"bound": "tensor", "achieved": round(value / world, 2), "peak": pk * (4 if w4a4 else 1),
-                         "unit": "TFLOP/s", "frac": round(value / world / (pk * (4 if w4a4 else 1)), 4),
-                         "peak_source": src + (" bf16 x 4 (nominal fp4 ratio)" if w4a4 else ""), "traffic": None},
-            "per_gemm_tflops_median": by, "clocks": clk, "gpu_launches": len(per) * (3 if w4a4 else 1)}
+            "config": {"workload": r["what"] + ": encoder Linears qkvo/fc1/fc2 at M=1500*B, B in {1,4,16}",
+                       "l2": "flushed (256 MB write) before every launch, outside the timed events"},
+            "roofline": {"bound": "tensor", "achieved": r["value"], "peak": r["peak"], "unit": "TFLOP/s",
+                         "frac": r["frac_of_peak"], "peak_source": src + (f" bf16 x {FP4_OVER_BF16:g}" if w4a4 else ""),
+                         "traffic": None},
+            "per_gemm_tflops_median": r["per_gemm_tflops_median"], "clocks": clk,
+            "gpu_launches": 9 * args.steps * (3 if w4a4 else 1)}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -472,43 +741,80 @@ _ORACLE_CACHE = {}
 
 
 def _oracle_inputs():
-    """Oracle-packed weights and fp32 inputs of the decoder sweep (built once, not timed)."""
+    """Oracle-packed weights and fp32 inputs of the decoder sweep (built once; the packing time of
+    the 40 weights is recorded)."""
     if "items" not in _ORACLE_CACHE:
         from bit_weight_quantized_matmul_gb300 import workloads as wl
         from oracle import quant as Q
         linears, Ms = decoder_workload()
-        items = []
+        items, t_pack, pack_bytes = [], 0.0, 0
         for l in linears:
-            p = Q.nf4_pack(wl.weight(l["seed"], l["N"], l["K"]))
+            W = wl.weight(l["seed"], l["N"], l["K"])
+            t0 = time.perf_counter()
+            p = Q.nf4_pack(W)
+            t_pack += time.perf_counter() - t0
+            pack_bytes += W.nbytes
             b = wl.bf16_as_f32(wl.bias(l["seed"], l["N"])) if l["bias"] else None
             for M in Ms:
                 x = wl.bf16_as_f32(wl.activations(l["seed"] * 7 + M, M, l["K"]))
                 items.append((l, M, p, x, b))
         _ORACLE_CACHE["items"] = items
+        _ORACLE_CACHE["pack"] = {"seconds": round(t_pack, 3), "weights": len(linears),
+                                 "GBps_of_fp32_weights": round(pack_bytes / t_pack / 1e9, 4),
+                                 "what": "oracle NF4 pack + double-quant of the 40 decoder weights (single-threaded numpy)"}
     return _ORACLE_CACHE["items"]
 
 
 def cpu_baseline(seconds=15.0):
     """The oracle (numpy NF4 decode + fp64 matmul, as it stands) on a bounded sample of the
     same workload: whole passes over the step's 120 Linear-calls, repeated until ``seconds``
-    of CPU work (a partial pass at the end counts the Linears it finished)."""
+    of CPU work (a partial pass at the end counts the Linears it finished).  The NF4 decode is
+    timed apart from the fp64 matmul."""
     from oracle import linear as L
+    from oracle import quant as Q
     items = _oracle_inputs()
-    done_bytes, t_total, n = 0, 0.0, 0
+    done_bytes, t_total, t_dec, n = 0, 0.0, 0.0, 0
     while t_total < seconds:
         for l, M, p, x, b in items:
             t0 = time.perf_counter()
-            L.linear_w4a16(x, p, b)
-            t_total += time.perf_counter() - t0
+            w_hat = Q.nf4_dequant(p)
+            t1 = time.perf_counter()
+            L.linear_fp64(x, w_hat, b)
+            t2 = time.perf_counter()
+            t_total += t2 - t0
+            t_dec += t1 - t0
             done_bytes += nf4_linear_bytes(l["N"], l["K"], M, l["bias"])
             n += 1
             if t_total >= seconds:
                 break
-    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
-            "kind": "oracle",
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{n} Linear-calls of the step's 120 (whole passes in order), numpy NF4 decode + "
                       f"fp64 matmul, {t_total:.1f} s of CPU time",
-            "threads_note": "numpy elementwise single-threaded; fp64 matmul on the BLAS thread pool"}
+            "decode_share": round(t_dec / t_total, 3),
+            "pack": _ORACLE_CACHE.get("pack"),
+            "threads_note": ("numpy elementwise single-threaded; fp64 matmul on the BLAS thread pool"
+                             if not threads else f"BLAS threads {threads}")}
+
+
+def cpu_baseline_one_core(seconds):
+    """The same oracle sample pinned to one core with one BLAS thread, in a child process (the
+    thread count of numpy's BLAS is fixed when numpy loads)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    env.pop("RANK", None), env.pop("WORLD_SIZE", None), env.pop("LOCAL_RANK", None)
+    code = ("import os, sys, json; os.sched_setaffinity(0, {min(os.sched_getaffinity(0))}); "
+            f"sys.path.insert(0, {ROOT!r}); import bench; "
+            f"print(json.dumps(bench.cpu_baseline({float(seconds)})))")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=seconds * 4 + 180)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": d["value"], "unit": "GB/s", "cores": d["cores"], "sample": d["sample"],
+                "decode_share": d["decode_share"]}
+    except Exception as e:  # the GPU line stays valid without it
+        return {"value": None, "error": str(e)[:200]}
 
 
 def run_reference(args, rank, world):
@@ -524,6 +830,7 @@ def run_reference(args, rank, world):
     vals = [cpu_baseline(seconds=per)["value"] for _ in range(args.steps)]
     elapsed = time.perf_counter() - t0
     v = statistics.median(vals)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"impl": "reference", "metric": "4-bit dequant-linear effective HBM bandwidth, decode (M<=16)",
             "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1000 * elapsed / max(1, args.steps), 3), "higher_is_better": True,
@@ -531,7 +838,7 @@ def run_reference(args, rank, world):
             "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": "whisper-large-v3-turbo decoder sweep: 4 layers x 10 NF4 Linears, "
                                    "M in {1,4,16}; each step a bounded sample of it"},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
                              "sample": f"{per:.2f} s of oracle work per step over the step's Linear-calls"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -541,10 +848,13 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--reps", type=int, default=200, help="individually timed replays for median / p10 / p90")
+    ap.add_argument("--clock-seconds", type=float, default=1.5, help="length of the clock-sampled window")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds-one-core", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--workload", default="decoder_nf4", choices=["decoder_nf4", "encoder_w4a16", "encoder_w4a4"])
     args = ap.parse_args()

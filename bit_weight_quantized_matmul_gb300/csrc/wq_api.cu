@@ -261,6 +261,14 @@ int wq_selftest_timeout(uint32_t polls, void* stream) {
   return wq::selftest_timeout(polls, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int wq_selftest_encoders(const float* in, int64_t n, uint8_t* out, void* stream) {
+  if (n < 0 || n > (int64_t(1) << 30)) return WQ_ERR_ARG;
+  if (n == 0) return WQ_OK;
+  if (!in || !out) return WQ_ERR_ARG;
+  if (!aligned16(in) || !aligned16(out)) return WQ_ERR_ALIGN;
+  return wq::selftest_encoders(in, n, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int wq_last_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
   int worst = WQ_OK;

@@ -37,6 +37,7 @@ int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, 
                     uint8_t* scales, float* g_out, cudaStream_t s);
 int take_status_pack();
 int selftest_timeout(uint32_t polls, cudaStream_t s);  // bounded wait on a barrier nobody arrives on
+int selftest_encoders(const float* in, int64_t n, uint8_t* out, cudaStream_t s);
 
 // ---- linear: CUDA-core path (wq_simt.cu)
 struct LinearArgs {

@@ -466,6 +466,40 @@ __global__ void selftest_timeout_kernel(uint32_t polls) {
   }
 }
 
+// Scalar-encoder self test: for each fp32 input, the library's own E2M1 and E4M3 encoders
+// (the ones the packers and the activation quantiser use) next to the hardware conversions
+// cvt.rn.satfinite.{e2m1x2,e4m3x2}.f32 on the same value, so a test can compare both with
+// the oracle (ties, signed zeros, subnormal and saturating scales).
+__global__ void selftest_encoders_kernel(const float* __restrict__ in, int64_t n, uint8_t* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float x = in[i];
+  uint32_t hw_e2m1, hw_e4m3;
+  // the converted value of the first source lands in the upper half, the second in the lower
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %1, %2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %1, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %1, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %1, %1;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(hw_e2m1)
+      : "f"(0.0f), "f"(x));
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(x));
+  hw_e4m3 = h & 0xFFu;
+  out[4 * i + 0] = (uint8_t)f32_to_e2m1(x);
+  out[4 * i + 1] = (uint8_t)(hw_e2m1 & 0xFu);
+  out[4 * i + 2] = (uint8_t)f32_to_e4m3_satfinite(x);
+  out[4 * i + 3] = (uint8_t)hw_e4m3;
+}
+
+int selftest_encoders(const float* in, int64_t n, uint8_t* out, cudaStream_t s) {
+  if (n == 0) return WQ_OK;
+  selftest_encoders_kernel<<<grid_for(n, 256), 256, 0, s>>>(in, n, out);
+  count_launch();
+  return launch_status();
+}
+
 int selftest_timeout(uint32_t polls, cudaStream_t s) {
   selftest_timeout_kernel<<<1, 32, 0, s>>>(polls);
   count_launch();

@@ -56,6 +56,7 @@ _SIGS = {
     "wq_status_string": (ctypes.c_char_p, [_I]),
     "wq_kernel_launches": (ctypes.c_uint64, []),
     "wq_selftest_timeout": (_I, [ctypes.c_uint32, _P]),
+    "wq_selftest_encoders": (_I, [_P, _I64, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -195,3 +196,12 @@ def selftest_timeout(polls=1000, stream=None):
     """Run the bounded-wait failure path once (a barrier nobody arrives on); the next
     last_device_status() reports WQ_ERR_TIMEOUT."""
     _check("wq_selftest_timeout", lib.wq_selftest_timeout(polls, _stream(stream)))
+
+
+def selftest_encoders(x, stream=None):
+    """fp32 CUDA tensor x -> uint8 [n, 4]: (library E2M1, hardware E2M1, library E4M3,
+    hardware E4M3) codes of every value."""
+    assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
+    out = torch.empty((x.numel(), 4), dtype=torch.uint8, device=x.device)
+    _check("wq_selftest_encoders", lib.wq_selftest_encoders(_ptr(x), x.numel(), _ptr(out), _stream(stream)))
+    return out

@@ -201,6 +201,19 @@ uint64_t wq_kernel_launches(void);
  * arrives) without faulting the GPU.  WQ_ERR_ARG for polls out of range.    */
 int wq_selftest_timeout(uint32_t polls, void* stream);
 
+/* ---------------------------------------------------------------- encoder check
+ * wq_selftest_encoders: a verification export.  For each of the n fp32 values
+ * in[i] (device), writes four bytes out[4i .. 4i+3] (device):
+ *   [0] the E2M1 code the library's packers / activation quantiser assign
+ *   [1] the E2M1 code of the hardware conversion cvt.rn.satfinite.e2m1x2.f32
+ *   [2] the E4M3 byte the library's block-scale encoder assigns
+ *   [3] the E4M3 byte of cvt.rn.satfinite.e4m3x2.f32
+ * so that tests can pin both the library's encoders (model card
+ * "whisper-large-v3-turbo -- NVFP4", "What is quantized": E2M1 codes, E4M3
+ * block scales) and the hardware's rounding of ties and signed zeros.
+ * WQ_ERR_ARG for n < 0 or n > 2^30, WQ_ERR_ALIGN for unaligned pointers.     */
+int wq_selftest_encoders(const float* in, int64_t n, uint8_t* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
