@@ -28,6 +28,19 @@ Formats and the passages they follow
   q4_0 decodes as (q - 8) * d, q8_0 as q * d.  Readings: the codes are
   computed against the stored (fp16-rounded) d; q4_0's d maps the block's
   signed extreme to code 0 (d = extreme / -8).
+* q4_1 / q5_0 -- the same PR, "Why the policy" (the other GGUF block types,
+  slower there without fast kernels).  The pages name them only.  Readings:
+  GGUF's block definitions, blocks of 32 with fp16 scales: q4_1 stores d and
+  a minimum m and decodes as q * d + m (q in 0..15, d = (max - min) / 15,
+  m = min); q5_0 stores d and 5-bit codes and decodes as (q - 16) * d
+  (d = extreme / -16, the q4_0 rule with 16 levels a side).  Codes are
+  computed against the stored fp16 values, rounding half to even.
+* FP8 E4M3 weights -- model card "whisper-large-v3-turbo -- NVFP4", "Honest
+  summary" and "Why the encoder/decoder split matters" (the FP8 build and the
+  NVFP4-encoder / FP8-decoder build).  The card names the type only.
+  Reading: E4M3 codes with one fp32 scale per output row (weight row of W),
+  s = amax_row / 448, code = E4M3(w / s) round to nearest even, saturating;
+  decode E4M3(code) * s.
 """
 
 import math
@@ -218,9 +231,84 @@ def q8_0_dequant(p):
     return (q * p["d"].astype(np.float32)[:, None]).astype(np.float32).reshape(p["N"], p["K"])
 
 
+# ---------------------------------------------------------------- q4_1
+def q4_1_pack(W):
+    """Blocks of 32: m = fp16(min), d = fp16((max - min) / 15), q = clamp(rint((x - m) / d), 0, 15)
+    with the stored m and d (q = 0 where d == 0)."""
+    W = _f32(W)
+    N, K = W.shape
+    assert K % GGUF_BLOCK == 0
+    b = W.reshape(-1, GGUF_BLOCK)
+    mn = np.min(b, axis=1).astype(np.float32)
+    mx = np.max(b, axis=1).astype(np.float32)
+    d = F.fp16_round(((mx - mn).astype(np.float32) / np.float32(15)).astype(np.float32))
+    m = F.fp16_round(mn)
+    dq, mq = d.astype(np.float32), m.astype(np.float32)
+    safe = np.where(dq == 0, np.float32(1), dq)
+    t = (b - mq[:, None]).astype(np.float32)
+    q = np.clip(np.rint((t / safe[:, None]).astype(np.float32)), 0, 15)
+    q = np.where(dq[:, None] == 0, 0, q).astype(np.uint8)
+    return dict(fmt="q4_1", N=N, K=K, codes=q.reshape(-1), d=d, m=m)
+
+
+def q4_1_dequant(p):
+    """x_hat = q * d + m: the product is exact in fp32 (4-bit q, 11-bit d), the sum rounds once."""
+    q = p["codes"].astype(np.float32).reshape(-1, GGUF_BLOCK)
+    prod = (q * p["d"].astype(np.float32)[:, None]).astype(np.float32)
+    return (prod + p["m"].astype(np.float32)[:, None]).astype(np.float32).reshape(p["N"], p["K"])
+
+
+# ---------------------------------------------------------------- q5_0
+def q5_0_pack(W):
+    """Blocks of 32: d = fp16(extreme / -16) with the extreme the first element of largest |x|,
+    q = clamp(rint(x / d) + 16, 0, 31) with the stored d (q = 16 where d == 0)."""
+    W = _f32(W)
+    N, K = W.shape
+    assert K % GGUF_BLOCK == 0
+    b = W.reshape(-1, GGUF_BLOCK)
+    idx = np.argmax(np.abs(b), axis=1)
+    extreme = b[np.arange(b.shape[0]), idx]
+    d = F.fp16_round((extreme / np.float32(-16)).astype(np.float32))
+    dq = d.astype(np.float32)
+    safe = np.where(dq == 0, np.float32(1), dq)
+    q = np.clip(np.rint((b / safe[:, None]).astype(np.float32)) + 16, 0, 31)
+    q = np.where(dq[:, None] == 0, 16, q).astype(np.uint8)
+    return dict(fmt="q5_0", N=N, K=K, codes=q.reshape(-1), d=d)
+
+
+def q5_0_dequant(p):
+    q = p["codes"].astype(np.float32).reshape(-1, GGUF_BLOCK)
+    return ((q - np.float32(16)) * p["d"].astype(np.float32)[:, None]).astype(np.float32).reshape(p["N"], p["K"])
+
+
+# ---------------------------------------------------------------- FP8 E4M3 weights
+FP8_MAX = np.float32(448.0)
+
+
+def fp8_pack(W):
+    """One fp32 scale per row s = amax_row / 448 (fp32 division); code = E4M3(w / s), round to nearest
+    even, saturating, sign copied; code 0 where s == 0."""
+    W = _f32(W)
+    N, K = W.shape
+    amax = np.max(np.abs(W), axis=1).astype(np.float32) if K else np.zeros(N, np.float32)
+    s = (amax / FP8_MAX).astype(np.float32)
+    safe = np.where(s == 0, np.float32(1), s)
+    codes = F.e4m3_encode_satfinite((W / safe[:, None]).astype(np.float32))
+    codes = np.where(s[:, None] == 0, np.uint8(0), codes).astype(np.uint8)
+    return dict(fmt="fp8", N=N, K=K, codes=codes.reshape(-1), s=s)
+
+
+def fp8_dequant(p):
+    """x_hat = E4M3(code) * s: one fp32 rounding."""
+    v = F.e4m3_decode(p["codes"]).reshape(p["N"], p["K"])
+    return (v * p["s"][:, None]).astype(np.float32)
+
+
 # ---------------------------------------------------------------- dispatch
-PACK = {"nf4": nf4_pack, "nvfp4": nvfp4_pack, "q4_0": q4_0_pack, "q8_0": q8_0_pack}
-DEQUANT = {"nf4": nf4_dequant, "nvfp4": nvfp4_dequant, "q4_0": q4_0_dequant, "q8_0": q8_0_dequant}
+PACK = {"nf4": nf4_pack, "nvfp4": nvfp4_pack, "q4_0": q4_0_pack, "q8_0": q8_0_pack,
+        "q4_1": q4_1_pack, "q5_0": q5_0_pack, "fp8": fp8_pack}
+DEQUANT = {"nf4": nf4_dequant, "nvfp4": nvfp4_dequant, "q4_0": q4_0_dequant, "q8_0": q8_0_dequant,
+           "q4_1": q4_1_dequant, "q5_0": q5_0_dequant, "fp8": fp8_dequant}
 
 
 # ---------------------------------------------------------------- byte blobs
@@ -235,13 +323,26 @@ def to_blobs(p):
             q8_0: one int8 per element.
     scales: nf4:   int8 absmax codes [N*K/64] | zero pad to 16 B | fp32 s2 [groups] | fp32 offset
             nvfp4: E4M3 bytes [N, K/16] row-major | zero pad to 16 B | fp32 g
-            q4_0 / q8_0: fp16 d [N*K/32] | zero pad to 16 B
+            q4_0 / q8_0 / q5_0: fp16 d [N*K/32] | zero pad to 16 B
+            q4_1:  (fp16 d, fp16 m) pairs [N*K/32] | zero pad to 16 B
+            fp8:   fp32 s [N] | zero pad to 16 B
+    q5_0 packed: per 128 consecutive elements of a row, 64 bytes of low nibbles (element 2j in the
+            low nibble of byte j) then 16 bytes of high bits (bit j of byte i is the fifth bit of
+            element 8i + j of the 128).
     """
     fmt = p["fmt"]
-    if fmt in ("nf4", "nvfp4", "q4_0"):
+    if fmt in ("nf4", "nvfp4", "q4_0", "q4_1"):
         packed = pack_nibbles(p["codes"]).tobytes()
-    else:
+    elif fmt == "q5_0":
+        assert p["K"] % 128 == 0, "q5_0 rows hold whole 128-element units"
+        c = np.asarray(p["codes"], np.uint8).reshape(-1, 128)
+        lo = pack_nibbles(c & 0xF).reshape(-1, 64)
+        hi = np.packbits((c >> 4).astype(np.uint8).reshape(-1, 16, 8), axis=2, bitorder="little").reshape(-1, 16)
+        packed = np.concatenate([lo, hi], axis=1).tobytes()
+    elif fmt == "q8_0":
         packed = np.asarray(p["codes"], np.int8).tobytes()
+    else:  # fp8
+        packed = np.asarray(p["codes"], np.uint8).tobytes()
     if fmt == "nf4":
         a = np.asarray(p["absmax_q"], np.int8).tobytes()
         scales = a + b"\0" * (_align16(len(a)) - len(a))
@@ -249,6 +350,12 @@ def to_blobs(p):
     elif fmt == "nvfp4":
         s = np.asarray(p["scales"], np.uint8).tobytes()
         scales = s + b"\0" * (_align16(len(s)) - len(s)) + np.float32(p["g"]).tobytes()
+    elif fmt == "q4_1":
+        dm = np.stack([np.asarray(p["d"], np.float16), np.asarray(p["m"], np.float16)], axis=1).tobytes()
+        scales = dm + b"\0" * (_align16(len(dm)) - len(dm))
+    elif fmt == "fp8":
+        sv = np.asarray(p["s"], np.float32).tobytes()
+        scales = sv + b"\0" * (_align16(len(sv)) - len(sv))
     else:
         d = np.asarray(p["d"], np.float16).tobytes()
         scales = d + b"\0" * (_align16(len(d)) - len(d))
