@@ -34,7 +34,14 @@ ScalesLayout scales_layout(int fmt, int64_t N, int64_t K) {
       break;
     case WQ_Q4_0:
     case WQ_Q8_0:
+    case WQ_Q5_0:
       L.total = align16((size_t)(n / 32) * 2);
+      break;
+    case WQ_Q4_1:
+      L.total = align16((size_t)(n / 32) * 4);
+      break;
+    case WQ_FP8:
+      L.total = align16((size_t)N * 4);
       break;
     default:
       break;
@@ -88,7 +95,10 @@ int block_of(int fmt) {
     case WQ_NVFP4:
     case WQ_NVFP4_W4A4: return 32;  // 16-blocks; rows of packed codes must stay 16-byte aligned
     case WQ_Q4_0:
-    case WQ_Q8_0: return 32;
+    case WQ_Q8_0:
+    case WQ_Q4_1:
+    case WQ_FP8: return 32;
+    case WQ_Q5_0: return 128;  // whole 128-element storage units per row
     default: return 0;
   }
 }
@@ -118,7 +128,7 @@ extern "C" {
 
 size_t wq_packed_bytes(int fmt, int64_t N, int64_t K) {
   if (check_weight(fmt, N, K) != WQ_OK) return 0;
-  return fmt == WQ_Q8_0 ? (size_t)(N * K) : (size_t)(N * K / 2);
+  return (size_t)(N * packed_row_bytes(fmt, K));
 }
 
 size_t wq_scales_bytes(int fmt, int64_t N, int64_t K) {
@@ -137,6 +147,16 @@ int wq_pack_q4_0(const float* W, int64_t N, int64_t K, void* packed, void* scale
 }
 int wq_pack_q8_0(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream) {
   return pack_common(WQ_Q8_0, W, N, K, packed, scales, stream, pack_q8_0);
+}
+
+int wq_pack_q4_1(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream) {
+  return pack_common(WQ_Q4_1, W, N, K, packed, scales, stream, pack_q4_1);
+}
+int wq_pack_q5_0(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream) {
+  return pack_common(WQ_Q5_0, W, N, K, packed, scales, stream, pack_q5_0);
+}
+int wq_pack_fp8(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream) {
+  return pack_common(WQ_FP8, W, N, K, packed, scales, stream, pack_fp8);
 }
 
 int wq_dequant(const void* packed, const void* scales, int fmt, int64_t N, int64_t K, float* W_out, void* stream) {

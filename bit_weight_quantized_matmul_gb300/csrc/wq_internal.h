@@ -19,6 +19,15 @@ struct ScalesLayout {
   size_t g_off = 0;         // NVFP4: byte offset of the fp32 g
   size_t total = 0;
 };
+// Packed bytes of one weight row (K elements) of a format.
+inline int64_t packed_row_bytes(int fmt, int64_t K) {
+  switch (fmt) {
+    case WQ_Q8_0:
+    case WQ_FP8: return K;
+    case WQ_Q5_0: return K / 128 * 80;
+    default: return K / 2;
+  }
+}
 ScalesLayout scales_layout(int fmt, int64_t N, int64_t K);
 
 inline size_t align16(size_t n) { return (n + 15) / 16 * 16; }
@@ -31,6 +40,9 @@ int pack_nf4(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* sca
 int pack_nvfp4(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s);
 int pack_q4_0(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s);
 int pack_q8_0(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s);
+int pack_q4_1(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s);
+int pack_q5_0(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s);
+int pack_fp8(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s);
 int dequant(const uint8_t* packed, const uint8_t* scales, int fmt, int64_t N, int64_t K, float* out,
             cudaStream_t s);
 int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, uint8_t* codes,

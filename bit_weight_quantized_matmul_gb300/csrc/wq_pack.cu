@@ -344,15 +344,123 @@ __global__ void q8_0_kernel(const float* __restrict__ W, int64_t nb, int8_t* __r
   d_out[b] = __half_as_ushort(d16);
 }
 
+// q4_1: m = fp16(min), d = fp16((max - min) / 15), q = clamp(rint((x - m) / d), 0, 15) against the
+// stored m and d (q = 0 where d == 0); scales hold (d, m) fp16 pairs.
+__global__ void q4_1_kernel(const float* __restrict__ W, int64_t nb, uint8_t* __restrict__ packed,
+                            uint32_t* __restrict__ dm_out) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0)
+    for (int64_t i = nb; i % 4 != 0; ++i) dm_out[i] = 0u;  // zero the pad to 16 bytes
+  if (b >= nb) return;
+  const float4* src = reinterpret_cast<const float4*>(W + b * kGGBlock);
+  float v[kGGBlock];
+  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kGGBlock / 4; ++i) {
+    const float4 t = src[i];
+    v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+  }
+#pragma unroll
+  for (int i = 0; i < kGGBlock; ++i) { mn = fminf(mn, v[i]); mx = fmaxf(mx, v[i]); }
+  const __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
+  const __half m16 = __float2half_rn(mn);
+  const float d = __half2float(d16), m = __half2float(m16);
+  uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < kGGBlock; ++i) {
+    float q = 0.0f;
+    if (d != 0.0f) q = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[i], m), d)), 0.0f), 15.0f);
+    w[i >> 3] |= ((uint32_t)q) << (4 * (i & 7));
+  }
+  reinterpret_cast<uint4*>(packed)[b] = make_uint4(w[0], w[1], w[2], w[3]);
+  dm_out[b] = (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(m16) << 16);
+}
+
+// q5_0: d = fp16(extreme / -16), q = clamp(rint(x / d) + 16, 0, 31) (q = 16 where d == 0).  Storage
+// unit of 128 elements: 64 bytes of low nibbles, then 16 bytes of fifth bits; block b of a unit owns
+// nibble bytes [16b, 16b + 16) and fifth-bit bytes [64 + 4b, 64 + 4b + 4).
+__global__ void q5_0_kernel(const float* __restrict__ W, int64_t nb, uint8_t* __restrict__ packed,
+                            uint16_t* __restrict__ d_out) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0) zero_d_pad(d_out, nb);
+  if (b >= nb) return;
+  const float4* src = reinterpret_cast<const float4*>(W + b * kGGBlock);
+  float v[kGGBlock];
+#pragma unroll
+  for (int i = 0; i < kGGBlock / 4; ++i) {
+    const float4 t = src[i];
+    v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+  }
+  float best = -1.0f, ext = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kGGBlock; ++i)
+    if (fabsf(v[i]) > best) { best = fabsf(v[i]); ext = v[i]; }  // strict: first index wins ties
+  const __half d16 = __float2half_rn(__fdiv_rn(ext, -16.0f));
+  const float d = __half2float(d16);
+  uint32_t w[4] = {0, 0, 0, 0}, hb = 0;
+#pragma unroll
+  for (int i = 0; i < kGGBlock; ++i) {
+    float q = 16.0f;
+    if (d != 0.0f) q = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(v[i], d)), 16.0f), 0.0f), 31.0f);
+    const uint32_t qi = (uint32_t)q;
+    w[i >> 3] |= (qi & 15u) << (4 * (i & 7));
+    hb |= (qi >> 4) << i;
+  }
+  const int64_t unit = b / 4, blk = b % 4;
+  uint8_t* base = packed + unit * 80;
+  *reinterpret_cast<uint4*>(base + 16 * blk) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint32_t*>(base + 64 + 4 * blk) = hb;
+  d_out[b] = __half_as_ushort(d16);
+}
+
+// FP8 E4M3 weights, one warp per row: s = amax(row) / 448, q = E4M3(w / s) (0 where s == 0).
+__global__ void fp8_kernel(const float* __restrict__ W, int64_t N, int64_t K, uint8_t* __restrict__ packed,
+                           float* __restrict__ s_out, int pad_words) {
+  const int64_t n = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (n == 0 && lane < pad_words) s_out[N + lane] = 0.0f;  // zero the pad to 16 bytes
+  if (n >= N) return;
+  const float* row = W + n * K;
+  float a = 0.0f;
+  for (int64_t k = 4 * lane; k < K; k += 128) {
+    const float4 t = *reinterpret_cast<const float4*>(row + k);
+    a = fmaxf(a, fmaxf(fmaxf(fabsf(t.x), fabsf(t.y)), fmaxf(fabsf(t.z), fabsf(t.w))));
+  }
+  a = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(a)));
+  const float sc = __fdiv_rn(a, 448.0f);
+  if (lane == 0) s_out[n] = sc;
+  for (int64_t k = 4 * lane; k < K; k += 128) {
+    const float4 t = *reinterpret_cast<const float4*>(row + k);
+    const float x[4] = {t.x, t.y, t.z, t.w};
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w |= (sc == 0.0f ? 0u : f32_to_e4m3_satfinite(__fdiv_rn(x[j], sc))) << (8 * j);
+    *reinterpret_cast<uint32_t*>(packed + n * K + k) = w;
+  }
+}
+
 // ------------------------------------------------------------------ dequant export
 // one thread per 8 consecutive elements
 __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales, int fmt,
-                               int64_t n8, ScalesLayout lay, float* __restrict__ out) {
+                               int64_t n8, int64_t K, ScalesLayout lay, float* __restrict__ out) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= n8) return;
   const int64_t e0 = t * 8;
   float r[8];
-  if (fmt == WQ_Q8_0) {
+  if (fmt == WQ_FP8) {
+    const uint2 c = reinterpret_cast<const uint2*>(packed)[t];
+    const float sc = reinterpret_cast<const float*>(scales)[e0 / K];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[j] = __fmul_rn(e4m3_to_f32(((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFFu), sc);
+  } else if (fmt == WQ_Q5_0) {
+    const int64_t unit = e0 / 128, off = e0 % 128;
+    const uint32_t c = *reinterpret_cast<const uint32_t*>(packed + unit * 80 + off / 2);
+    const uint32_t hb = packed[unit * 80 + 64 + off / 8];
+    const float d = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(scales)[e0 / kGGBlock]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      r[j] = __fmul_rn((float)((int)(((c >> (4 * j)) & 15u) | (((hb >> j) & 1u) << 4)) - 16), d);
+  } else if (fmt == WQ_Q8_0) {
     const uint2 c = reinterpret_cast<const uint2*>(packed)[t];
     const float d = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(scales)[e0 / kGGBlock]);
 #pragma unroll
@@ -375,6 +483,11 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t
       const float g = *reinterpret_cast<const float*>(scales + lay.g_off);
 #pragma unroll
       for (int j = 0; j < 8; ++j) r[j] = __fmul_rn(__fmul_rn(kE2M1[(c >> (4 * j)) & 15u], s), g);
+    } else if (fmt == WQ_Q4_1) {
+      const uint32_t dm = reinterpret_cast<const uint32_t*>(scales)[e0 / kGGBlock];
+      const float d = f16_bits_to_f32(dm & 0xFFFFu), m = f16_bits_to_f32(dm >> 16);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) r[j] = __fadd_rn(__fmul_rn((float)((c >> (4 * j)) & 15u), d), m);
     } else {  // q4_0
       const float d = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(scales)[e0 / kGGBlock]);
 #pragma unroll
@@ -441,11 +554,35 @@ int pack_q8_0(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* sc
   return launch_status();
 }
 
+int pack_q4_1(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s) {
+  const int64_t nb = N * K / kGGBlock;
+  if (nb == 0) return WQ_OK;
+  q4_1_kernel<<<grid_for(nb, 128), 128, 0, s>>>(W, nb, packed, reinterpret_cast<uint32_t*>(scales));
+  count_launch();
+  return launch_status();
+}
+
+int pack_q5_0(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s) {
+  const int64_t nb = N * K / kGGBlock;
+  if (nb == 0) return WQ_OK;
+  q5_0_kernel<<<grid_for(nb, 128), 128, 0, s>>>(W, nb, packed, reinterpret_cast<uint16_t*>(scales));
+  count_launch();
+  return launch_status();
+}
+
+int pack_fp8(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales, cudaStream_t s) {
+  if (N * K == 0) return WQ_OK;
+  const int pad_words = (int)((align16((size_t)N * 4) - (size_t)N * 4) / 4);
+  fp8_kernel<<<grid_for(N, 8), 256, 0, s>>>(W, N, K, packed, reinterpret_cast<float*>(scales), pad_words);
+  count_launch();
+  return launch_status();
+}
+
 int dequant(const uint8_t* packed, const uint8_t* scales, int fmt, int64_t N, int64_t K, float* out,
             cudaStream_t s) {
   const int64_t n8 = N * K / 8;
   if (n8 == 0) return WQ_OK;
-  dequant_kernel<<<grid_for(n8, 256), 256, 0, s>>>(packed, scales, fmt, n8, scales_layout(fmt, N, K), out);
+  dequant_kernel<<<grid_for(n8, 256), 256, 0, s>>>(packed, scales, fmt, n8, K, scales_layout(fmt, N, K), out);
   count_launch();
   return launch_status();
 }

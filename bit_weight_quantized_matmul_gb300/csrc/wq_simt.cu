@@ -35,6 +35,23 @@ struct SimtParams {
 // 8 consecutive weights of row n starting at column k (k % 8 == 0), exact fp32
 __device__ __forceinline__ void decode8(const SimtParams& p, int64_t n, int64_t k, float (&w)[8]) {
   const int64_t e0 = n * p.K + k;
+  if (p.fmt == WQ_FP8) {
+    const uint2 c = *reinterpret_cast<const uint2*>(p.packed + e0);
+    const float sc = reinterpret_cast<const float*>(p.scales)[n];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = __fmul_rn(e4m3_to_f32(((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFFu), sc);
+    return;
+  }
+  if (p.fmt == WQ_Q5_0) {
+    const int64_t unit = e0 / 128, off = e0 % 128;
+    const uint32_t c = *reinterpret_cast<const uint32_t*>(p.packed + unit * 80 + off / 2);
+    const uint32_t hb = p.packed[unit * 80 + 64 + off / 8];
+    const float d = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.scales)[e0 / 32]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      w[j] = __fmul_rn((float)((int)(((c >> (4 * j)) & 15u) | (((hb >> j) & 1u) << 4)) - 16), d);
+    return;
+  }
   if (p.fmt == WQ_Q8_0) {
     const uint2 c = *reinterpret_cast<const uint2*>(p.packed + e0);
     const float d = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.scales)[e0 / 32]);
@@ -51,6 +68,11 @@ __device__ __forceinline__ void decode8(const SimtParams& p, int64_t n, int64_t 
     const float a = __fadd_rn(__fmul_rn((float)q, s2), off);
 #pragma unroll
     for (int j = 0; j < 8; ++j) w[j] = __fmul_rn(kNF4[(c >> (4 * j)) & 15u], a);
+  } else if (p.fmt == WQ_Q4_1) {
+    const uint32_t dm = reinterpret_cast<const uint32_t*>(p.scales)[e0 / 32];
+    const float d = f16_bits_to_f32(dm & 0xFFFFu), m = f16_bits_to_f32(dm >> 16);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = __fadd_rn(__fmul_rn((float)((c >> (4 * j)) & 15u), d), m);
   } else if (p.fmt == WQ_Q4_0) {
     const float d = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.scales)[e0 / 32]);
 #pragma unroll

@@ -58,7 +58,8 @@ struct Smem {
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tmem base, abort flag
   static constexpr int RED_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
   static constexpr int RED_BYTES = (BN <= 16) ? kRows * (BN + 1) * 4 : 0;
-  static constexpr int TOTAL = RED_OFF + RED_BYTES + 1024;  // + alignment slack
+  static constexpr int RB_OFF = RED_OFF + RED_BYTES;          // fp32 bias per tile row
+  static constexpr int TOTAL = RB_OFF + kRows * 4 + 1024;     // + alignment slack
 };
 
 template <int BN>
@@ -165,13 +166,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t n = (int64_t)n0 + r;
     const bool row_ok = n < p.N;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    // Values that do not depend on the preceding kernel are requested before the first weight
+    // tile lands, so their memory latency overlaps the weight stream's: the scale words of the
+    // first kPre chunks of this row, the bias and the NVFP4 global scale.
+    constexpr int kPre = 8;
+    uint32_t sw[kPre];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i)
+      sw[i] = (i < nchunks && row_ok) ? scale_word<FMT>(p.scales, p.lay, p.K, n, kc_begin + i) : 0u;
+    const float gsc = (FMT == WQ_NVFP4) ? *reinterpret_cast<const float*>(p.scales + p.lay.g_off) : 1.0f;
+    const float bval = (p.bias && row_ok) ? bf16_bits_to_f32(p.bias[n]) : 0.0f;
+    float* row_bias = reinterpret_cast<float*>(smem + S::RB_OFF);  // for the split-K reduction
+    row_bias[r] = bval;
     for (int i = 0; i < nchunks; ++i) {
       const int s = i % STAGES, slot = i % kNA;
+      uint32_t word = 0u;
+#pragma unroll
+      for (int j = 0; j < kPre; ++j)
+        if (j == i) word = sw[j];
+      if (i >= kPre && row_ok) word = scale_word<FMT>(p.scales, p.lay, p.K, n, kc_begin + i);
       if (!mbar_wait(&full[s], (i / STAGES) & 1, abort_flag)) break;
       if (i >= kNA && !mbar_wait(&aempty[slot], ((i / kNA) & 1) ^ 1, abort_flag)) break;
+      constexpr int NW = Fmt<FMT>::WB / 16;  // 16-byte pieces of one row's 64 codes
+      const uint4* src = reinterpret_cast<const uint4*>(smem + S::W_OFF + s * S::WB + r * Fmt<FMT>::WB);
+      uint4 wv[NW];
+#pragma unroll
+      for (int k = 0; k < NW; ++k) wv[k] = src[k];
       uint32_t v[32];
-      decode_chunk<FMT>(p.scales, p.K, p.lay, smem + S::W_OFF + s * S::WB + r * Fmt<FMT>::WB, lut, n,
-                        (int64_t)(kc_begin + i) * kKS, row_ok, v);
+      decode_span<FMT, 64, 1>(word, 0, wv, lut, 0, v);
       tmem_st32(tmem_base + lane_base + slot * 32, v);
       tc_wait_st();
       tc_fence_before();
@@ -183,9 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool have_d = mbar_wait(dfull, 0, abort_flag);
     tc_fence_after();
     griddep_wait();
-    float gsc = 1.0f;
-    if (FMT == WQ_NVFP4) gsc = *reinterpret_cast<const float*>(p.scales + p.lay.g_off);
-    const float bval = (p.bias && row_ok) ? bf16_bits_to_f32(p.bias[n]) : 0.0f;
     float* red = reinterpret_cast<float*>(smem + S::RED_OFF);
     if (have_d) {
 #pragma unroll 1
@@ -225,18 +244,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r_lo = (int)(rank * kRows / ks), r_hi = (int)((rank + 1) * kRows / ks);
       const int rows = r_hi - r_lo;
       const int mcount = (p.M - m0) < BN ? (p.M - m0) : BN;
-      float gsc = 1.0f;
-      if (FMT == WQ_NVFP4) gsc = *reinterpret_cast<const float*>(p.scales + p.lay.g_off);
+      const float gsc = (FMT == WQ_NVFP4) ? *reinterpret_cast<const float*>(p.scales + p.lay.g_off) : 1.0f;
+      const float* row_bias = reinterpret_cast<const float*>(smem + S::RB_OFF);
       const uint32_t red_base = smem_u32(smem + S::RED_OFF);
       for (int idx = (int)threadIdx.x - 64; idx < rows * mcount; idx += 128) {
         const int j = idx / rows, rr = r_lo + idx % rows;
         const int64_t n = (int64_t)n0 + rr;
         if (n >= p.N) continue;
         const uint32_t off = red_base + (uint32_t)((rr * (BN + 1) + j) * 4);
+        // every peer's partial is requested before the first is added, so the remote loads overlap
+        // instead of paying the distributed-shared-memory latency once per peer
+        float part[8];
+#pragma unroll
+        for (int pr = 0; pr < 8; ++pr)
+          part[pr] = pr < ks ? ld_shared_cluster_f32(map_shared_rank(off, (uint32_t)pr)) : 0.0f;
         float sum = 0.0f;
-        for (int pr = 0; pr < ks; ++pr) sum += ld_shared_cluster_f32(map_shared_rank(off, (uint32_t)pr));
-        const float bval = p.bias ? bf16_bits_to_f32(p.bias[n]) : 0.0f;
-        const float val = __fadd_rn(__fmul_rn(sum, gsc), bval);
+#pragma unroll
+        for (int pr = 0; pr < 8; ++pr) sum += part[pr];
+        const float val = __fadd_rn(__fmul_rn(sum, gsc), row_bias[rr]);
         const int64_t m = m0 + j;
         if (p.out_f32)
           reinterpret_cast<float*>(p.y)[m * p.N + n] = val;

@@ -34,73 +34,6 @@ __device__ __forceinline__ float nibble_value(uint32_t c) {
   return kE2M1[c];  // NVFP4: E2M1 value; the E4M3 block scale multiplies it, g is applied on D
 }
 
-// Decode the 64 weights [k0, k0 + 64) of row n into 32 bf16x2 words.
-template <int FMT>
-__device__ __forceinline__ void decode_chunk(const uint8_t* __restrict__ scales, int64_t K, const ScalesLayout& lay,
-                                             const uint8_t* wrow, const float2* lut, int64_t n, int64_t k0,
-                                             bool row_ok, uint32_t (&out)[32]) {
-  if (FMT == WQ_Q8_0) {
-    float d0 = 0.0f, d1 = 0.0f;
-    if (row_ok) {
-      const uint32_t dd = *reinterpret_cast<const uint32_t*>(scales + 2 * ((n * K + k0) / 32));
-      d0 = f16_bits_to_f32(dd & 0xFFFFu);
-      d1 = f16_bits_to_f32(dd >> 16);
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(wrow);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = src[q];
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-      const float d = (q < 2) ? d0 : d1;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a0 = (float)(int8_t)(u[j] & 0xFF), a1 = (float)(int8_t)((u[j] >> 8) & 0xFF);
-        const float a2 = (float)(int8_t)((u[j] >> 16) & 0xFF), a3 = (float)(int8_t)(u[j] >> 24);
-        out[q * 8 + j * 2] = pack_bf16x2(__fmul_rn(a0, d), __fmul_rn(a1, d));
-        out[q * 8 + j * 2 + 1] = pack_bf16x2(__fmul_rn(a2, d), __fmul_rn(a3, d));
-      }
-    }
-    return;
-  }
-  // 4-bit formats: 32 bytes, element 2j in the low nibble of byte j
-  float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // scale per 16 elements of the chunk
-  if (row_ok) {
-    if (FMT == WQ_NF4) {
-      const int64_t b = (n * K + k0) / 64;
-      const int8_t q = reinterpret_cast<const int8_t*>(scales)[b];
-      const float s2 = reinterpret_cast<const float*>(scales + lay.s2_off)[b / 256];
-      const float off = *reinterpret_cast<const float*>(scales + lay.offset_off);
-      const float a = __fadd_rn(__fmul_rn((float)q, s2), off);
-      sc[0] = sc[1] = sc[2] = sc[3] = a;
-    } else if (FMT == WQ_Q4_0) {
-      const uint32_t dd = *reinterpret_cast<const uint32_t*>(scales + 2 * ((n * K + k0) / 32));
-      sc[0] = sc[1] = f16_bits_to_f32(dd & 0xFFFFu);
-      sc[2] = sc[3] = f16_bits_to_f32(dd >> 16);
-    } else {  // NVFP4
-      const uint32_t s4 = *reinterpret_cast<const uint32_t*>(scales + (n * K + k0) / 16);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sc[j] = e4m3_to_f32((s4 >> (8 * j)) & 0xFFu);
-    }
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(wrow);
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint4 v = src[q];
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int byte_idx = q * 16 + j * 4 + b;  // elements 2*byte_idx, 2*byte_idx + 1
-        const float2 lv = lut[(u[j] >> (8 * b)) & 0xFFu];
-        const float s = sc[byte_idx >> 3];
-        out[byte_idx] = pack_bf16x2(__fmul_rn(lv.x, s), __fmul_rn(lv.y, s));
-      }
-    }
-  }
-}
-
-
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),

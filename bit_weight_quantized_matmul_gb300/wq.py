@@ -21,8 +21,9 @@ if not os.path.exists(LIB_PATH):
 lib = ctypes.CDLL(LIB_PATH)
 
 # ------------------------------------------------------------------ constants
-WQ_NF4, WQ_NVFP4, WQ_NVFP4_W4A4, WQ_Q4_0, WQ_Q8_0 = 1, 2, 3, 4, 5
-FMT = {"nf4": WQ_NF4, "nvfp4": WQ_NVFP4, "nvfp4_w4a4": WQ_NVFP4_W4A4, "q4_0": WQ_Q4_0, "q8_0": WQ_Q8_0}
+WQ_NF4, WQ_NVFP4, WQ_NVFP4_W4A4, WQ_Q4_0, WQ_Q8_0, WQ_Q4_1, WQ_Q5_0, WQ_FP8 = 1, 2, 3, 4, 5, 6, 7, 8
+FMT = {"nf4": WQ_NF4, "nvfp4": WQ_NVFP4, "nvfp4_w4a4": WQ_NVFP4_W4A4, "q4_0": WQ_Q4_0, "q8_0": WQ_Q8_0,
+       "q4_1": WQ_Q4_1, "q5_0": WQ_Q5_0, "fp8": WQ_FP8}
 WQ_OK, WQ_ERR_ARG, WQ_ERR_SHAPE, WQ_ERR_ALIGN, WQ_ERR_FMT, WQ_ERR_CUDA, WQ_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 WQ_FLAG_OUT_F32, WQ_FLAG_WEIGHTS_STATIC, WQ_FLAG_FORCE_SIMT = 1, 2, 4
 
@@ -47,6 +48,9 @@ _SIGS = {
     "wq_pack_nvfp4": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "wq_pack_q4_0": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "wq_pack_q8_0": (_I, [_P, _I64, _I64, _P, _P, _P]),
+    "wq_pack_q4_1": (_I, [_P, _I64, _I64, _P, _P, _P]),
+    "wq_pack_q5_0": (_I, [_P, _I64, _I64, _P, _P, _P]),
+    "wq_pack_fp8": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "wq_dequant": (_I, [_P, _P, _I, _I64, _I64, _P, _P]),
     "wq_quant_act_nvfp4": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _P]),
     "wq_linear": (_I, [_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
@@ -107,7 +111,8 @@ def alloc_packed(fmt, N, K, device="cuda"):
 
 
 _PACK_FN = {"nf4": "wq_pack_nf4", "nvfp4": "wq_pack_nvfp4", "nvfp4_w4a4": "wq_pack_nvfp4",
-            "q4_0": "wq_pack_q4_0", "q8_0": "wq_pack_q8_0"}
+            "q4_0": "wq_pack_q4_0", "q8_0": "wq_pack_q8_0", "q4_1": "wq_pack_q4_1", "q5_0": "wq_pack_q5_0",
+            "fp8": "wq_pack_fp8"}
 
 
 def pack(fmt, W, out=None, stream=None):

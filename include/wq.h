@@ -46,7 +46,10 @@ typedef enum wq_fmt {
   WQ_NVFP4 = 2,      /* E2M1 codes, block 16, E4M3 block scale, fp32 global; bf16 activations   */
   WQ_NVFP4_W4A4 = 3, /* NVFP4 weights AND NVFP4 activations (see wq_act_nvfp4)                   */
   WQ_Q4_0 = 4,       /* 4-bit codes, block 32, fp16 d, value (q - 8) * d                        */
-  WQ_Q8_0 = 5        /* int8 codes, block 32, fp16 d, value q * d                               */
+  WQ_Q8_0 = 5,       /* int8 codes, block 32, fp16 d, value q * d                               */
+  WQ_Q4_1 = 6,       /* 4-bit codes, block 32, fp16 d and fp16 minimum m, value q * d + m       */
+  WQ_Q5_0 = 7,       /* 5-bit codes, block 32, fp16 d, value (q - 16) * d                       */
+  WQ_FP8 = 8         /* FP8 E4M3 codes, one fp32 scale s per weight row, value E4M3(q) * s      */
 } wq_fmt;
 
 typedef enum wq_status {
@@ -73,14 +76,20 @@ typedef struct wq_act_nvfp4 {
 /* ---------------------------------------------------------------- sizes
  * Bytes of the two buffers a packed weight occupies (0 for an invalid
  * format / shape).  Storage layout:
- *   packed  NF4, NVFP4, q4_0: N*K/2 bytes, two codes per byte, element 2j of
- *           the row-major flattening in the low nibble of byte j.
- *           q8_0: N*K int8.
+ *   packed  NF4, NVFP4, q4_0, q4_1: N*K/2 bytes, two codes per byte, element
+ *           2j of the row-major flattening in the low nibble of byte j.
+ *           q8_0: N*K int8.  FP8: N*K E4M3 bytes.
+ *           q5_0: N*K*5/8 bytes: per 128 consecutive elements of a row, 64
+ *           bytes of low nibbles (element 2j in the low nibble of byte j) then
+ *           16 bytes of fifth bits (bit j of byte i = element 8i + j).
  *   scales  NF4:   int8 absmax codes [N*K/64] | zero pad to 16 B |
  *                  fp32 second-level scale s2 [ceil(N*K/64 / 256)] | fp32 offset
  *           NVFP4: E4M3 block scales [N, K/16] row-major | zero pad to 16 B | fp32 g
- *           q4_0, q8_0: fp16 d [N*K/32] | zero pad to 16 B
- * Size rules: NF4 K % 64 == 0; NVFP4 K % 32 == 0; q4_0 / q8_0 K % 32 == 0.   */
+ *           q4_0, q8_0, q5_0: fp16 d [N*K/32] | zero pad to 16 B
+ *           q4_1:  (fp16 d, fp16 m) pairs [N*K/32] | zero pad to 16 B
+ *           FP8:   fp32 s [N] | zero pad to 16 B
+ * Size rules: NF4 K % 64 == 0; NVFP4 K % 32 == 0; q4_0 / q8_0 / q4_1 / FP8
+ * K % 32 == 0; q5_0 K % 128 == 0.                                             */
 size_t wq_packed_bytes(int fmt, int64_t N, int64_t K);
 size_t wq_scales_bytes(int fmt, int64_t N, int64_t K);
 
@@ -102,16 +111,29 @@ size_t wq_scales_bytes(int fmt, int64_t N, int64_t K);
  * wq_pack_q4_0  (PR "Run quantized Whisper on the fused Metal decode path",
  *   "Summary"): d = fp16(extreme / -8), q = clamp(rint(w / d) + 8, 0, 15).
  * wq_pack_q8_0  (same passage): d = fp16(amax / 127), q = clamp(rint(w / d), +-127).
+ * wq_pack_q4_1, wq_pack_q5_0 (same PR, "Why the policy": the other GGUF block
+ *   types): q4_1 m = fp16(min), d = fp16((max - min) / 15),
+ *   q = clamp(rint((w - m) / d), 0, 15); q5_0 d = fp16(extreme / -16),
+ *   q = clamp(rint(w / d) + 16, 0, 31).
+ * wq_pack_fp8   (model card "whisper-large-v3-turbo -- NVFP4", "Honest
+ *   summary": the FP8 build): s = amax(row) / 448, q = E4M3(w / s), round to
+ *   nearest even, saturating (q = 0 for an all-zero row).
+ * Every rint / E4M3 rounding is half to even, against the stored fp16 / fp32
+ * scale values.
  */
 int wq_pack_nf4(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream);
 int wq_pack_nvfp4(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream);
 int wq_pack_q4_0(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream);
 int wq_pack_q8_0(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream);
+int wq_pack_q4_1(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream);
+int wq_pack_q5_0(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream);
+int wq_pack_fp8(const float* W, int64_t N, int64_t K, void* packed, void* scales, void* stream);
 
 /* ---------------------------------------------------------------- dequant
  * Decode a packed weight to fp32 W_out [N, K] (device): the exact fp32 value
  * each code stands for (NF4: codebook * (q*s2 + offset); NVFP4:
- * (E2M1 * E4M3) * g; q4_0: (q-8)*d; q8_0: q*d).  A verification export: the
+ * (E2M1 * E4M3) * g; q4_0: (q-8)*d; q8_0: q*d; q4_1: q*d + m; q5_0:
+ * (q-16)*d; FP8: E4M3(q)*s).  A verification export: the
  * fused paths below never materialise W.                                       */
 int wq_dequant(const void* packed, const void* scales, int fmt, int64_t N, int64_t K,
                float* W_out, void* stream);

@@ -259,3 +259,43 @@ def test_nf4_codebook_midpoints_and_neighbours():
     # the fixture's midpoints really are ties: those elements got the lower code
     codes = ref["codes"].reshape(4, 128)
     assert list(codes[0, 1:16]) == list(range(15))
+
+
+def test_fp8_weight_worked_matrix_and_ties():
+    """The hand-worked FP8 matrix (E4M3 ties, subnormals, the tie to zero, -0), and rows whose
+    w / s lands exactly on every E4M3 midpoint (s = 1: the row amax is 448)."""
+    need_gpu()
+    g = golden_dict("fp8_worked.txt")
+    W = np.zeros((6, 288), np.float32)
+    x0 = [float(v) for v in g["x0"][0]]
+    W[0, :len(x0)] = x0
+    W[0, 10] = -0.0
+    W[1] = W[0] * 2
+    x3 = [float(v) for v in g["x3"][0]]
+    W[3, :len(x3)] = x3
+    mids = ((F.E4M3_FINITE_POS[:-1] + F.E4M3_FINITE_POS[1:]) / 2).astype(np.float32)   # 126 values
+    W[4, 0] = 448.0
+    W[4, 1:1 + mids.size] = mids
+    W[4, 128:128 + mids.size] = -mids
+    W[5, 0] = -448.0
+    W[5, 1:1 + mids.size] = np.nextafter(mids, np.float32(0))
+    W[5, 128:128 + mids.size] = np.nextafter(mids, np.float32(1e9))
+    _check_pack("fp8", W)
+
+
+@pytest.mark.parametrize("golden", ["q4_1_worked.txt", "q5_0_worked.txt"])
+def test_other_gguf_worked_rows(golden):
+    """The hand-worked q4_1 and q5_0 rows (rint ties both ways, the clamp side, -0 scales of
+    all-zero blocks) through the GPU packers."""
+    need_gpu()
+    g = golden_dict(golden)
+    fmt = golden.split("_worked")[0]
+    W = np.zeros((1, 128), np.float32)
+    if fmt == "q4_1":
+        W[0, :32] = float(g["rest0"][0][0])
+        W[0, 32:64] = float(g["rest1"][0][0])
+    x0 = [float(v) for v in g["x0"][0]]
+    x1 = [float(v) for v in g["x1"][0]]
+    W[0, :len(x0)] = x0
+    W[0, 32:32 + len(x1)] = x1
+    _check_pack(fmt, np.concatenate([W, -W, W * np.float32(0.25)]))

@@ -63,6 +63,7 @@ def run_case(fmt, M, N, K, seed=0, has_bias=True, outliers=0.0, force_simt=False
 
 
 FMTS = ["nf4", "nvfp4", "q4_0", "q8_0"]
+NEW_FMTS = ["q4_1", "q5_0", "fp8"]
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -153,3 +154,12 @@ def test_w4a4_tensor_path_is_exact_products(M, K):
     got = y.cpu().numpy().astype(np.float64)
     bound = (K * 2.0 ** -24 + 2.0 ** -22) * (np.abs(x_hat) @ np.abs(w_hat).T) + 1e-30
     assert np.all(np.abs(got - y_ref) <= bound), float(np.max(np.abs(got - y_ref) / bound))
+
+
+@pytest.mark.parametrize("fmt", NEW_FMTS)
+@pytest.mark.parametrize("M,N,K", [(1, 1280, 1280), (4, 5120, 1280), (16, 1280, 5120), (3, 200, 384),
+                                   (300, 1280, 1280), (37, 640, 5120)])
+def test_other_block_types(fmt, M, N, K):
+    """q4_1, q5_0 (the other GGUF block types) and FP8 E4M3 weights, decode and encoder sizes."""
+    need_gpu()
+    run_case(fmt, M, N, K, seed=7 * M + N + K)

@@ -17,11 +17,14 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("fmt", ["nf4", "nvfp4", "q4_0", "q8_0"])
+BLOCK = {"nf4": 64, "nvfp4": 32, "q4_0": 32, "q8_0": 32, "q4_1": 32, "q5_0": 128, "fp8": 32}
+
+
+@pytest.mark.parametrize("fmt", ["nf4", "nvfp4", "q4_0", "q8_0", "q4_1", "q5_0", "fp8"])
 @pytest.mark.parametrize("N,K", SHAPES)
 def test_pack_and_dequant_bit_exact(fmt, N, K):
     need_gpu()
-    if K % (64 if fmt == "nf4" else 32):
+    if K % BLOCK[fmt]:
         pytest.skip("shape not valid for format")
     W = weight_np(N * 7 + K, N, K)
     W[0, :16] *= 30.0                  # an outlier block
