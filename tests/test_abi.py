@@ -44,7 +44,8 @@ def test_library_exports_every_declared_symbol(wq):
 
 @pytest.mark.parametrize("fmt,N,K", [("nf4", 1536, 384), ("nf4", 3, 6400), ("nf4", 1280, 1280),
                                      ("nvfp4", 1280, 5120), ("nvfp4", 2, 32), ("q4_0", 384, 1536),
-                                     ("q8_0", 5120, 1280), ("q8_0", 1, 32)])
+                                     ("q8_0", 5120, 1280), ("q8_0", 1, 32), ("q4_1", 3, 96), ("q4_1", 1280, 1280),
+                                     ("q5_0", 5, 384), ("q5_0", 1280, 5120), ("fp8", 3, 32), ("fp8", 1280, 1280)])
 def test_sizes_match_oracle_blobs(wq, fmt, N, K):
     W = np.random.default_rng(0).standard_normal((N, K)).astype(np.float32) * 0.02
     packed, scales = Q.to_blobs(Q.PACK[fmt](W))
@@ -57,6 +58,8 @@ def test_size_rules(wq):
     assert wq.packed_bytes("q4_0", 4, 48) == 0         # K % 32
     assert wq.packed_bytes("nvfp4", 4, 48) == 0        # K % 32 (16-blocks, 16-byte rows)
     assert wq.packed_bytes(9, 4, 64) == 0              # unknown format
+    assert wq.packed_bytes("q5_0", 4, 64) == 0         # K % 128 (whole storage units)
+    assert wq.packed_bytes("q5_0", 4, 256) == 4 * 160 and wq.packed_bytes("fp8", 3, 64) == 192
     assert wq.packed_bytes("nf4", 0, 64) == 0 and wq.scales_bytes("q8_0", 0, 32) == 0
 
 
@@ -68,7 +71,8 @@ def test_argument_checks_before_any_launch(wq):
     assert L.wq_pack_nf4(None, 4, 64, fake, fake, None) == wq.WQ_ERR_ARG
     assert L.wq_pack_q8_0(odd, 4, 64, fake, fake, None) == wq.WQ_ERR_ALIGN
     assert L.wq_pack_nvfp4(fake, -1, 64, fake, fake, None) == wq.WQ_ERR_ARG
-    assert L.wq_linear(fake, fake, fake, 7, 1, 4, 64, None, fake, None) == wq.WQ_ERR_FMT
+    assert L.wq_linear(fake, fake, fake, 9, 1, 4, 64, None, fake, None) == wq.WQ_ERR_FMT
+    assert L.wq_linear(fake, fake, fake, wq.WQ_Q5_0, 1, 4, 64, None, fake, None) == wq.WQ_ERR_SHAPE
     assert L.wq_linear(None, fake, fake, wq.WQ_NF4, 1, 4, 64, None, fake, None) == wq.WQ_ERR_ARG
     assert L.wq_linear(fake, fake, fake, wq.WQ_NF4, 1, 4, 96, None, fake, None) == wq.WQ_ERR_SHAPE
     assert L.wq_linear(odd, fake, fake, wq.WQ_NF4, 1, 4, 64, None, fake, None) == wq.WQ_ERR_ALIGN
