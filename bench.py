@@ -457,6 +457,7 @@ def run_ours(args, rank, local_rank, world):
     if rank == 0 and not args.no_extra:
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         out["per_linear"] = per_linear(torch, wq, T, flush, linears, copies, xs, ys, biases, Ms)
+        out["decode_layer"] = decode_layer(torch, wq, T, dev, linears, copies, xs, ys, biases)
         del copies, packed0
         torch.cuda.empty_cache()
         out["extra"] = extra_lines(args, torch, wq, wl, dev, T, flush, peaks)
@@ -500,6 +501,53 @@ def per_linear(torch, wq, T, flush, linears, copies, xs, ys, biases, Ms):
                 "isolated_us_median": round(1000 * pct(iso, 50), 3),
                 "isolated_GBps": round(nb / (pct(iso, 50) * 1e-3) / 1e9, 1), "launches": len(calls)}
             del g
+    return res
+
+
+def decode_layer(torch, wq, T, dev, linears, copies, xs, ys, biases, Ms=(1, 4)):
+    """One decoder layer per token as a real decode step launches it (cross-attention K/V come from
+    the encoder once per window, so a token runs self q, k, v, o, cross q, o, fc1 and fc2): each
+    Linear its own wq_linear launch, against the fused form whose self-attention Q/K/V is one
+    wq_linear_grouped_ex launch writing K and V straight into row t of KV-cache slabs.  All 4 layers x
+    9 weight copies in one CUDA graph (weights from HBM), time per layer-token."""
+    per_layer, t = 10, 7
+    slab_k = torch.zeros((64, 1280), dtype=torch.bfloat16, device=dev)
+    slab_v = torch.zeros((64, 1280), dtype=torch.bfloat16, device=dev)
+    res = {}
+    for M in Ms:
+        def single(c, i):
+            p, s = copies[c][i]
+            wq.linear_into(ys[M][i], xs[M][i], p, s, "nf4", linears[i]["N"], linears[i]["K"], biases[i],
+                           weights_static=True)
+
+        def unfused(c, layer):
+            for j in (0, 1, 2, 3, 4, 7, 8, 9):
+                single(c, layer * per_layer + j)
+
+        def fused(c, layer):
+            i0 = layer * per_layer
+            probs = []
+            for j, out in ((0, ys[M][i0]), (1, slab_k[t:t + M]), (2, slab_v[t:t + M])):
+                p, s = copies[c][i0 + j]
+                probs.append((xs[M][i0], p, s, 1280, 1280, biases[i0 + j], [(out, 1280)]))
+            wq.linear_grouped_ex(probs, "nf4", weights_static=True)
+            for j in (3, 4, 7, 8, 9):
+                single(c, i0 + j)
+
+        row = {"launches_per_layer_unfused": 8, "launches_per_layer_fused": 6}
+        for name, fn in (("unfused", unfused), ("fused_qkv", fused)):
+            with torch.cuda.stream(T.stream):
+                fn(0, 0)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=T.stream):
+                for c in range(len(copies)):
+                    for layer in range(4):
+                        fn(c, layer)
+            tm = T.region(lambda k: g.replay(), 3) / 3
+            row[f"{name}_us_per_layer"] = round(1000 * tm / (4 * len(copies)), 3)
+            del g
+        res[f"M{M}"] = row
     return res
 
 

@@ -81,6 +81,19 @@ bool encode_tmap_2d(void* tmap, CUtensorMapDataType dtype, const void* base, uin
   return r == CUDA_SUCCESS;
 }
 
+int linear_one(const LinearArgs& a, cudaStream_t s) {
+  int rc = WQ_OK;
+  const bool dense = a.nout == 1 && a.ld[0] == a.N;
+  if (a.fmt == WQ_NVFP4_W4A4) {
+    if (dense && linear_w4a4_tc(a, s, &rc)) return rc;
+  } else if (a.M <= 16) {
+    if (gemv_eligible(a)) return linear_gemv(a, s);
+    if (dense && linear_tc(a, s, &rc)) return rc;
+  }
+  if (a.fmt != WQ_NVFP4_W4A4 && tcp_eligible(a)) return linear_tcp(&a, 1, s);
+  return linear_simt(a, s);
+}
+
 }  // namespace wq
 
 using namespace wq;
@@ -211,40 +224,69 @@ int wq_linear_ex(const void* x, const void* packed, const void* scales, int fmt,
   a.K = K;
   a.bias = bias;
   a.y = y;
+  set_single_out(a);
   a.out_f32 = (flags & WQ_FLAG_OUT_F32) != 0;
   a.weights_static = (flags & WQ_FLAG_WEIGHTS_STATIC) != 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (!(flags & WQ_FLAG_FORCE_SIMT)) {
-    if (fmt == WQ_NVFP4_W4A4) {
-      if (linear_w4a4_tc(a, s, &rc)) return rc;
-    } else if (M <= 16) {
-      if (linear_tc(a, s, &rc)) return rc;
-    } else if (tcp_eligible(a)) {
-      return linear_tcp(&a, 1, s);
-    }
-  }
-  return linear_simt(a, s);
+  if (flags & WQ_FLAG_FORCE_SIMT) return linear_simt(a, s);
+  return linear_one(a, s);
 }
 
 int wq_linear_grouped(const wq_problem* problems, int count, int fmt, unsigned flags, void* stream) {
   if (!problems || count < 1 || count > WQ_GROUP_MAX) return WQ_ERR_ARG;
+  wq_problem_ex ex[WQ_GROUP_MAX];
+  for (int i = 0; i < count; ++i) {
+    const wq_problem& p = problems[i];
+    ex[i] = wq_problem_ex{};
+    ex[i].x = p.x;
+    ex[i].packed = p.packed;
+    ex[i].scales = p.scales;
+    ex[i].bias = p.bias;
+    ex[i].M = p.M;
+    ex[i].N = p.N;
+    ex[i].K = p.K;
+    ex[i].nout = 1;
+    ex[i].out[0] = wq_out{p.y, p.N, p.N};
+  }
+  return wq_linear_grouped_ex(ex, count, fmt, flags, stream);
+}
+
+int wq_linear_grouped_ex(const wq_problem_ex* problems, int count, int fmt, unsigned flags, void* stream) {
+  if (!problems || count < 1 || count > WQ_GROUP_MAX) return WQ_ERR_ARG;
   if (flags & ~(unsigned)(WQ_FLAG_OUT_F32 | WQ_FLAG_WEIGHTS_STATIC)) return WQ_ERR_ARG;
   if (fmt == WQ_NVFP4_W4A4) return WQ_ERR_FMT;
+  const size_t esz = (flags & WQ_FLAG_OUT_F32) ? 4 : 2;
   LinearArgs args[WQ_GROUP_MAX];
   int n = 0;
   bool all_tc = true;
   for (int i = 0; i < count; ++i) {
-    const wq_problem& p = problems[i];
+    const wq_problem_ex& p = problems[i];
     int rc = check_weight(fmt, p.N, p.K);
     if (rc != WQ_OK) return rc;
     if (p.M < 0) return WQ_ERR_ARG;
+    if (p.nout < 1 || p.nout > WQ_OUT_MAX) return WQ_ERR_ARG;
     if (p.M == 0 || p.N == 0) continue;
-    if (!p.x || !p.packed || !p.scales || !p.y) return WQ_ERR_ARG;
-    if (!aligned16(p.x) || !aligned16(p.packed) || !aligned16(p.scales) || !aligned16(p.y) ||
-        (p.bias && !aligned16(p.bias)))
+    if (!p.x || !p.packed || !p.scales) return WQ_ERR_ARG;
+    if (!aligned16(p.x) || !aligned16(p.packed) || !aligned16(p.scales) || (p.bias && !aligned16(p.bias)))
       return WQ_ERR_ALIGN;
     LinearArgs a{};
+    int64_t c = 0;
+    for (int d = 0; d < p.nout; ++d) {
+      const wq_out& o = p.out[d];
+      if (!o.y || o.ncols <= 0 || o.ld < o.ncols) return WQ_ERR_ARG;
+      if (d + 1 < p.nout && o.ncols % 16 != 0) return WQ_ERR_ARG;
+      if (!aligned16(o.y) || ((size_t)o.ld * esz) % 16 != 0) return WQ_ERR_ALIGN;
+      if (o.ld > 0x7FFFFFFF) return WQ_ERR_SHAPE;
+      c += o.ncols;
+      a.ys[d] = o.y;
+      a.ld[d] = o.ld;
+      a.col_end[d] = c;
+    }
+    if (c != p.N) return WQ_ERR_ARG;
+    a.nout = p.nout;
+    for (int d = p.nout; d < WQ_OUT_MAX; ++d) { a.ys[d] = a.ys[p.nout - 1]; a.ld[d] = a.ld[p.nout - 1]; a.col_end[d] = c; }
     a.x = p.x;
+    a.y = p.out[0].y;
     a.packed = reinterpret_cast<const uint8_t*>(p.packed);
     a.scales = reinterpret_cast<const uint8_t*>(p.scales);
     a.fmt = fmt;
@@ -252,7 +294,6 @@ int wq_linear_grouped(const wq_problem* problems, int count, int fmt, unsigned f
     a.N = p.N;
     a.K = p.K;
     a.bias = p.bias;
-    a.y = p.y;
     a.out_f32 = (flags & WQ_FLAG_OUT_F32) != 0;
     a.weights_static = (flags & WQ_FLAG_WEIGHTS_STATIC) != 0;
     all_tc = all_tc && tcp_eligible(a);
@@ -261,11 +302,8 @@ int wq_linear_grouped(const wq_problem* problems, int count, int fmt, unsigned f
   if (n == 0) return WQ_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (all_tc) return linear_tcp(args, n, s);
-  for (int i = 0; i < n; ++i) {  // some problem outside the tensor-core rules: one call each
-    const wq_problem& p = problems[i];
-    int rc = wq_linear_ex(args[i].x, args[i].packed, args[i].scales, fmt, args[i].M, args[i].N, args[i].K,
-                          args[i].bias, args[i].y, flags, stream);
-    (void)p;
+  for (int i = 0; i < n; ++i) {  // some problem outside the tensor-core rules: one launch each
+    const int rc = linear_one(args[i], s);
     if (rc != WQ_OK) return rc;
   }
   return WQ_OK;

@@ -62,12 +62,32 @@ struct LinearArgs {
   int fmt;
   int64_t M, N, K;
   const uint16_t* bias;
-  void* y;
+  void* y;                     // single output [M, N] (nout == 1, ld == N)
   bool out_f32;
   bool weights_static;         // may launch with programmatic dependent launch
+  // Output destinations: columns [col_end[d-1], col_end[d]) of row m go to
+  // ys[d] + m * ld[d] + (n - col_end[d-1]) (elements).  set_single_out() fills one destination.
+  int nout;
+  void* ys[WQ_OUT_MAX];
+  int64_t ld[WQ_OUT_MAX];
+  int64_t col_end[WQ_OUT_MAX];
 };
+inline void set_single_out(LinearArgs& a) {
+  a.nout = 1;
+  a.ys[0] = a.y;
+  a.ld[0] = a.N;
+  a.col_end[0] = a.N;
+  for (int d = 1; d < WQ_OUT_MAX; ++d) { a.ys[d] = a.y; a.ld[d] = a.N; a.col_end[d] = a.N; }
+}
+// One Linear of any shape and output layout: the tensor-core paths where their rules hold,
+// else the CUDA-core kernel.
+int linear_one(const LinearArgs& a, cudaStream_t s);
 int linear_simt(const LinearArgs& a, cudaStream_t s);
 int take_status_simt();
+
+// ---- linear: decode-sized single Linear on the CUDA cores (wq_gemv.cu)
+bool gemv_eligible(const LinearArgs& a);
+int linear_gemv(const LinearArgs& a, cudaStream_t s);
 
 // ---- linear: tensor-core paths (wq_tc.cu: decode split-K; wq_tcp.cu: persistent work list;
 //      wq_w4a4.cu: block-scaled FP4)

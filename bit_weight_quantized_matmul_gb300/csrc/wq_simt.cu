@@ -28,7 +28,9 @@ struct SimtParams {
   int fmt;
   int64_t M, N, K;
   const uint16_t* bias;
-  void* y;
+  void* ys[WQ_OUT_MAX];     // columns [col_end[d-1], col_end[d]) of row m at ys[d] + m * ld[d] + (n - col_end[d-1])
+  int64_t ld[WQ_OUT_MAX];
+  int64_t col_end[WQ_OUT_MAX];
   int out_f32;
 };
 
@@ -136,12 +138,16 @@ __global__ void __launch_bounds__(256) linear_simt_kernel(SimtParams p) {
   }
   if (lane == 0) {
     const float b = p.bias ? bf16_bits_to_f32(p.bias[n]) : 0.0f;
+    int d = 0;
+    while (d + 1 < WQ_OUT_MAX && n >= p.col_end[d]) ++d;
+    const int64_t col = n - (d ? p.col_end[d - 1] : 0);
     for (int i = 0; i < kMT && m0 + i < p.M; ++i) {
       const float v = acc[i] + b;
+      const int64_t off = (m0 + i) * p.ld[d] + col;
       if (p.out_f32)
-        reinterpret_cast<float*>(p.y)[(m0 + i) * p.N + n] = v;
+        reinterpret_cast<float*>(p.ys[d])[off] = v;
       else
-        reinterpret_cast<__nv_bfloat16*>(p.y)[(m0 + i) * p.N + n] = __float2bfloat16_rn(v);
+        reinterpret_cast<__nv_bfloat16*>(p.ys[d])[off] = __float2bfloat16_rn(v);
     }
   }
 }
@@ -163,7 +169,12 @@ int linear_simt(const LinearArgs& a, cudaStream_t s) {
   p.N = a.N;
   p.K = a.K;
   p.bias = a.bias;
-  p.y = a.y;
+  for (int d = 0; d < WQ_OUT_MAX; ++d) {
+    const int dd = d < a.nout ? d : a.nout - 1;
+    p.ys[d] = a.ys[dd];
+    p.ld[d] = a.ld[dd];
+    p.col_end[d] = a.col_end[dd];
+  }
   p.out_f32 = a.out_f32 ? 1 : 0;
   const int warps = 8;
   dim3 grid((unsigned)((a.N + warps - 1) / warps), (unsigned)((a.M + kMT - 1) / kMT));

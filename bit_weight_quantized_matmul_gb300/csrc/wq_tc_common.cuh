@@ -12,7 +12,11 @@ constexpr int kRows = 128; // weight rows per tile (the MMA M)
 
 template <int FMT>
 struct Fmt {
-  static constexpr int WB = (FMT == WQ_Q8_0) ? 64 : 32;  // packed bytes per row per stage
+  static constexpr bool BYTE = FMT == WQ_Q8_0 || FMT == WQ_FP8;  // one byte per weight
+  static constexpr int WB = BYTE ? 64 : 32;                        // packed bytes per row per 64 weights
+  // bytes per row and 64-block of the per-block scales staged for a tile (FP8: none, its one
+  // scale per row is applied in the epilogue)
+  static constexpr int SCB = FMT == WQ_NF4 ? 1 : FMT == WQ_FP8 ? 0 : 4;
 };
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -276,6 +280,33 @@ __device__ __forceinline__ void store_slab_bf16(const float (&acc)[16], float gs
       d4[1] = s4[1];
     } else {
       for (int e = 0; e < 16 && n + e < N; ++e) reinterpret_cast<uint16_t*>(dst)[e] = src[e];
+    }
+  }
+}
+}  // namespace tc
+}  // namespace wq
+
+namespace wq {
+namespace tc {
+// FP8 E4M3: decode NE codes (one byte each) into exact bf16 pairs.  The E4M3 sign, exponent and
+// mantissa fields placed at the bf16 bit positions (exponent field unchanged, mantissa shifted up
+// by four) make the bf16 number E4M3(code) * 2^-120, subnormals included (an E4M3 subnormal lands
+// on a bf16 subnormal with the same significand), and one bf16 multiply by 2^120 restores the
+// value exactly.  The per-row scale is applied to the fp32 accumulator in the epilogue.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t spread) {  // bytes in bits [0,8), [16,24)
+  const uint32_t bits = ((spread << 4) & 0x07F007F0u) | ((spread << 8) & 0x80008000u);
+  return hmul2_bf16(bits, 0x7B807B80u);  // x 2^120 in both halves
+}
+
+template <int NE>
+__device__ __forceinline__ void decode_span_fp8(const uint4* wv, uint32_t (&out)[NE / 2]) {
+#pragma unroll
+  for (int q = 0; q < NE / 16; ++q) {
+    const uint32_t u[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      out[q * 8 + j * 2] = e4m3x2_to_bf16x2(prmt(u[j], 0u, 0x4140u));
+      out[q * 8 + j * 2 + 1] = e4m3x2_to_bf16x2(prmt(u[j], 0u, 0x4342u));
     }
   }
 }

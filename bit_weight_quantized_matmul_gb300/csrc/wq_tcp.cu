@@ -67,15 +67,59 @@ constexpr int kMaxCtas = 160;     // persistent grid: one CTA per SM (152 on GB3
 constexpr int kMaxChunks = 80;    // 64-element blocks per row: K <= 5120 on this path
 constexpr int kS2Max = 48;        // NF4: s2 values a tile can touch (128 * 80 / 256 + 2) + offset
 
+struct PLay {  // the offsets of the scales blob the kernel reads (see ScalesLayout)
+  uint32_t s2_off, offset_off, g_off;
+};
+
 struct PProblem {
   const uint8_t* scales;
   const uint16_t* bias;
-  void* y;
+  void* y[WQ_OUT_MAX];      // output destinations: columns [col_end[d-1], col_end[d]) of row m at
+  int ld[WQ_OUT_MAX];       // y[d] + m * ld[d] + (n - col_end[d-1]) elements
+  int col_end[WQ_OUT_MAX];
   int M, N, K;
   int ntiles, mtiles;
   int item_begin;
-  ScalesLayout lay;
+  PLay lay;
 };
+
+// Output element (m, n) of problem pr: its address, given the element size.
+template <typename T>
+__device__ __forceinline__ T* out_ptr(const PProblem& pr, int64_t m, int64_t n) {
+  int d = 0;
+#pragma unroll
+  for (int i = 0; i < WQ_OUT_MAX - 1; ++i) d += (n >= pr.col_end[i]) ? 1 : 0;
+  const int64_t c0 = d ? pr.col_end[d - 1] : 0;
+  return reinterpret_cast<T*>(pr.y[d]) + m * pr.ld[d] + (n - c0);
+}
+
+// Store one 16-column slab of a D tile (TMEM lanes = 128 weight rows n0.., columns = 16 activation
+// rows m0..) through shared memory: each thread scales and writes its 16 values into stage[m][r],
+// then the threads copy the [16 x 128] bf16 slab out as 16-element runs of one output row with
+// 16-byte stores.  Destination boundaries are multiples of 16 columns, so a run never straddles two.
+__device__ __forceinline__ void store_slab_dest(const float (&acc)[16], float gsc, float bval, int r,
+                                                uint16_t* stage, const PProblem& pr, int64_t m0, int64_t n0) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float v = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
+    stage[j * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  epi_bar();
+  const int row = r >> 3, seg = (r & 7) * 16;
+  const int64_t m = m0 + row, n = n0 + seg;
+  if (m < pr.M && n < pr.N) {
+    uint16_t* dst = out_ptr<uint16_t>(pr, m, n);
+    const uint16_t* src = stage + row * 128 + seg;
+    if (n + 16 <= pr.N && ((uintptr_t)dst & 15u) == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      d4[0] = s4[0];
+      d4[1] = s4[1];
+    } else {
+      for (int e = 0; e < 16 && n + e < pr.N; ++e) dst[e] = src[e];
+    }
+  }
+}
 
 struct PParams {
   int nprob, total_items, out_f32, weights_static;
@@ -145,11 +189,11 @@ struct PSmem {
   static constexpr int FIXED = SC_OFF + 1024;                                   // + alignment slack
   // one tile's scale bytes as stored in the blob (row-major): 4 bytes per row per
   // 64-block (NVFP4 / q4_0 / q8_0), 1 byte (NF4); two buffers
-  static constexpr int sc_bytes(int blocks) { return blocks * kRows * (FMT == WQ_NF4 ? 1 : 4); }
+  static constexpr int sc_bytes(int blocks) { return blocks * kRows * Fmt<FMT>::SCB; }
   static constexpr int total(int blocks) { return FIXED + 2 * sc_bytes(blocks); }
   // the longest K (in 64-blocks) whose scale slices fit next to the pipeline
   static constexpr int max_blocks() {
-    const int fit = (227 * 1024 - FIXED) / (2 * kRows * (FMT == WQ_NF4 ? 1 : 4));
+    const int fit = Fmt<FMT>::SCB == 0 ? kMaxChunks : (227 * 1024 - FIXED) / (2 * kRows * Fmt<FMT>::SCB);
     return fit < kMaxChunks ? fit : kMaxChunks;
   }
   static_assert(max_blocks() >= 20, "shared memory budget: K = 1280 must fit");
@@ -194,8 +238,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   using S = PSmem<BN, STAGES, FMT, KC, LUTREP, MODE>;
   using T = PTmem<BN, KC, FMT, MODE>;
   static_assert(MODE != kScaleFold || (BN == 16 && FMT != WQ_NVFP4), "fold mode: decode tiles");
-  static_assert(MODE != kScaleBF16 || FMT == WQ_NVFP4, "bf16 scaling is exact for NVFP4 only");
-  static_assert(LUTREP != 0 || (FMT == WQ_NVFP4 && MODE == kScaleBF16), "register decode: NVFP4");
+  static_assert(MODE != kScaleBF16 || FMT == WQ_NVFP4 || FMT == WQ_FP8, "bf16 scaling is exact for NVFP4 only");
+  static_assert(LUTREP != 0 || ((FMT == WQ_NVFP4 || FMT == WQ_FP8) && MODE == kScaleBF16),
+                "register decode: NVFP4, FP8");
   constexpr bool FOLD = MODE == kScaleFold;
   constexpr int kNA = T::NA;
   // fold warps read chunk g's partials once A slot g % NA is released, and the partial
@@ -417,7 +462,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
           // the 64-block this warp decodes (NE >= 64), or the block holding its half (NE == 32)
           const int blk = (NE >= 64) ? (KC / 64) * c + NBW * h + bb : (KC / 64) * c + h / 2;
           sword[bb] = 0u;
-          if (!FOLD && row_ok && blk < nb) {
+          if (!FOLD && FMT != WQ_FP8 && row_ok && blk < nb) {
             if (FMT == WQ_NF4) {
               const int8_t qa = (int8_t)sc[r * nb + blk];
               const float s2 = s2s[(n * nb + blk) / 256 - g0];
@@ -431,7 +476,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         if (g >= kNA && !mbar_wait(&aempty[slot], ((g / kNA) & 1) ^ 1, abort_flag)) { ok = false; break; }
         const uint8_t* wstage = smem + S::W_OFF + s * S::WB;
         constexpr int NES = NE / NBW;                          // elements per decode call (32 or 64)
-        constexpr int CPS = NES / (FMT == WQ_Q8_0 ? 16 : 32);  // 16-byte chunks per call
+        constexpr int CPS = NES / (Fmt<FMT>::BYTE ? 16 : 32);  // 16-byte chunks per call
         const int ck0 = h * (WCHUNK / (16 * kDeqQ));            // first 16-byte chunk of this warp's part
 #pragma unroll
         for (int bb = 0; bb < NBW; ++bb) {
@@ -440,7 +485,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
 #pragma unroll
           for (int k = 0; k < CPS; ++k) wv[k] = load_wchunk<WRB, WNBOX>(wstage, r, ck0 + bb * CPS + k);
           const int part = (NE == 32) ? (h & 1) : 0;
-          if constexpr (LUTREP == 0)
+          if constexpr (FMT == WQ_FP8)
+            decode_span_fp8<NES>(wv, v);
+          else if constexpr (LUTREP == 0)
             decode_span_nvfp4_reg<NES>(sword[bb], part, wv, v);
           else if constexpr (MODE == kScaleF32)
             decode_span<FMT, NES, LUTREP>(sword[bb], part, wv, lut, lsel, v);
@@ -469,7 +516,10 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       const int buf = n_it % T::NDB;
       const int64_t n = (int64_t)ic.nt * kRows + r;
       const bool row_ok = n < pr.N;
-      const float gsc = (FMT == WQ_NVFP4) ? *reinterpret_cast<const float*>(pr.scales + pr.lay.g_off) : 1.0f;
+      // NVFP4: the tensor's global scale; FP8: the row's scale (0 past the last row)
+      const float gsc = (FMT == WQ_NVFP4) ? *reinterpret_cast<const float*>(pr.scales + pr.lay.g_off)
+                        : (FMT == WQ_FP8) ? (row_ok ? reinterpret_cast<const float*>(pr.scales)[n] : 0.0f)
+                                          : 1.0f;
       const float bval = (pr.bias && row_ok) ? bf16_bits_to_f32(pr.bias[n]) : 0.0f;
       const int m0 = ic.mt * BN;
       if (FOLD) {
@@ -530,9 +580,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
             if (m < pr.M) {
               const float val = __fadd_rn(acc[j], bval);
               if (P.out_f32)
-                reinterpret_cast<float*>(pr.y)[(int64_t)m * pr.N + n] = val;
+                *out_ptr<float>(pr, m, n) = val;
               else
-                reinterpret_cast<__nv_bfloat16*>(pr.y)[(int64_t)m * pr.N + n] = __float2bfloat16_rn(val);
+                *out_ptr<__nv_bfloat16>(pr, m, n) = __float2bfloat16_rn(val);
             }
           }
         }
@@ -547,14 +597,14 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         tmem_ld16(tmem_base + lane_base + T::D_COL + buf * BN + c0, acc);
         tc_wait_ld();
         if (!P.out_f32) {
-          store_slab_bf16(acc, gsc, bval, r, ystage + ((c0 / 16) & 1) * 16 * kRows, pr.y, pr.M, pr.N, m0 + c0,
+          store_slab_dest(acc, gsc, bval, r, ystage + ((c0 / 16) & 1) * 16 * kRows, pr, m0 + c0,
                           (int64_t)ic.nt * kRows);
         } else if (row_ok) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
             if (m < pr.M)
-              reinterpret_cast<float*>(pr.y)[(int64_t)m * pr.N + n] = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
+              *out_ptr<float>(pr, m, n) = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
           }
         }
       }
@@ -574,7 +624,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       if (n_it >= 2 && !mbar_wait(&sempty[sb], ((n_it >> 1) & 1) ^ 1, abort_flag)) break;
       const int64_t n0 = (int64_t)ic.nt * kRows;
       const int rows = (int)((pr.N - n0) < kRows ? (pr.N - n0) : kRows);
-      const int row_bytes = (FMT == WQ_NF4) ? nb : 4 * nb;
+      const int row_bytes = Fmt<FMT>::SCB * nb;
       // 16-byte aligned source (n0 * row_bytes is a multiple of 16) and a size rounded up to 16:
       // the scale regions of the blob are zero-padded to 16 bytes, so this stays inside it
       const uint32_t bytes = (uint32_t)(((int64_t)rows * row_bytes + 15) / 16 * 16);
@@ -586,7 +636,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         for (int64_t gi = g0 + lane; gi <= g1; gi += 32) s2s[gi - g0] = s2g[gi];
         if (lane == 0) s2s[kS2Max - 1] = *reinterpret_cast<const float*>(pr.scales + pr.lay.offset_off);
       }
-      if (lane == 0) {
+      if (lane == 0 && bytes > 0) {
         uint64_t* bar = &sfull[sb];
         mbar_arrive_expect_tx(bar, bytes);
         const uint8_t* src = pr.scales + n0 * row_bytes;
@@ -658,16 +708,24 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
     PProblem& pr = P.prob[j];
     pr.scales = a.scales;
     pr.bias = a.bias;
-    pr.y = a.y;
+    for (int d = 0; d < WQ_OUT_MAX; ++d) {
+      const int dd = d < a.nout ? d : a.nout - 1;
+      pr.y[d] = a.ys[dd];
+      pr.ld[d] = (int)a.ld[dd];
+      pr.col_end[d] = (int)a.col_end[dd];
+    }
     pr.M = (int)a.M;
     pr.N = (int)a.N;
     pr.K = (int)a.K;
     pr.ntiles = (int)((a.N + kRows - 1) / kRows);
     pr.mtiles = (int)((a.M + BN - 1) / BN);
     pr.item_begin = items;
-    pr.lay = scales_layout(FMT, a.N, a.K);
+    {
+      const ScalesLayout L = scales_layout(FMT, a.N, a.K);
+      pr.lay = PLay{(uint32_t)L.s2_off, (uint32_t)L.offset_off, (uint32_t)L.g_off};
+    }
     items += pr.ntiles * pr.mtiles;
-    const uint64_t wrow = (uint64_t)(FMT == WQ_Q8_0 ? a.K : a.K / 2);
+    const uint64_t wrow = (uint64_t)packed_row_bytes(FMT, a.K);
     if (!encode_tmap_2d(&maps.x[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M,
                         (uint64_t)a.K * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
       return WQ_ERR_CUDA;
@@ -746,7 +804,7 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
 // Decode is bound by the weight bytes in flight per SM: as many stages as shared memory holds
 // next to the scale slices of a K = 5120 tile (1 byte per row and 64-block for NF4, 4 for the
 // others; q8_0 stages are twice as large).
-constexpr int decode_stages(int fmt) { return fmt == WQ_NF4 ? 6 : fmt == WQ_Q8_0 ? 3 : 4; }
+constexpr int decode_stages(int fmt) { return fmt == WQ_NF4 ? 6 : (fmt == WQ_Q8_0 || fmt == WQ_FP8) ? 3 : 4; }
 constexpr int kGemmStagesP = 3;
 
 template <int FMT>
@@ -755,8 +813,9 @@ int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   for (int i = 0; i < count; ++i) maxM = std::max(maxM, probs[i].M);
   // NVFP4 decodes E2M1 in registers (no table) and scales exactly in bf16
   if (maxM <= 16) {
-    constexpr int mode = FMT == WQ_NVFP4 ? kScaleBF16 : kScaleFold;
-    constexpr int rep = FMT == WQ_NVFP4 ? 0 : 32;
+    constexpr bool reg = FMT == WQ_NVFP4 || FMT == WQ_FP8;  // register decode, exact bf16 scaling
+    constexpr int mode = reg ? kScaleBF16 : kScaleFold;
+    constexpr int rep = reg ? 0 : 32;
     static_assert(PSmem<16, decode_stages(FMT), FMT, 256, rep, mode>::max_blocks() >= kMaxChunks,
                   "decode tiles must take K = 5120");
     return launch_tcp<16, decode_stages(FMT), FMT, 256, rep, mode>(probs, count, out_f32, weights_static, s);
@@ -765,7 +824,7 @@ int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   // allows two stages of them and the scale slices of the longest K; else 128 rows (two accumulators)
   int64_t maxK = 0;
   for (int i = 0; i < count; ++i) maxK = std::max(maxK, probs[i].K);
-  if constexpr (FMT == WQ_NVFP4) {
+  if constexpr (FMT == WQ_NVFP4 || FMT == WQ_FP8) {
     using Wide = PSmem<256, 2, FMT, 128, 0, kScaleBF16>;
     if (maxK <= 64 * Wide::max_blocks())
       return launch_tcp<256, 2, FMT, 128, 0, kScaleBF16>(probs, count, out_f32, weights_static, s);
@@ -788,7 +847,7 @@ int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_st
 }  // namespace
 
 bool tcp_eligible(const LinearArgs& a) {
-  if (a.fmt != WQ_NF4 && a.fmt != WQ_NVFP4 && a.fmt != WQ_Q4_0 && a.fmt != WQ_Q8_0) return false;
+  if (a.fmt != WQ_NF4 && a.fmt != WQ_NVFP4 && a.fmt != WQ_Q4_0 && a.fmt != WQ_Q8_0 && a.fmt != WQ_FP8) return false;
   if (a.K % kKS != 0 || a.K < kKS || a.K > (int64_t)kKS * kMaxChunks) return false;
   if (a.M > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF) return false;
   return ((uintptr_t)a.x & 15u) == 0;
@@ -802,6 +861,7 @@ int linear_tcp(const LinearArgs* probs, int count, cudaStream_t s) {
     case WQ_NVFP4: return dispatch_p<WQ_NVFP4>(probs, count, out_f32, ws, s);
     case WQ_Q4_0: return dispatch_p<WQ_Q4_0>(probs, count, out_f32, ws, s);
     case WQ_Q8_0: return dispatch_p<WQ_Q8_0>(probs, count, out_f32, ws, s);
+    case WQ_FP8: return dispatch_p<WQ_FP8>(probs, count, out_f32, ws, s);
     default: return WQ_ERR_FMT;
   }
 }

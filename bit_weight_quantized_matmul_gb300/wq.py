@@ -39,6 +39,17 @@ class wq_problem(ctypes.Structure):
 
 
 WQ_GROUP_MAX = 48
+WQ_OUT_MAX = 4
+
+
+class wq_out(ctypes.Structure):
+    _fields_ = [("y", ctypes.c_void_p), ("ld", ctypes.c_int64), ("ncols", ctypes.c_int64)]
+
+
+class wq_problem_ex(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("nout", ctypes.c_int), ("out", wq_out * WQ_OUT_MAX)]
 
 _P, _I64, _I, _U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint
 _SIGS = {
@@ -56,6 +67,7 @@ _SIGS = {
     "wq_linear": (_I, [_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
     "wq_linear_ex": (_I, [_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _U, _P]),
     "wq_linear_grouped": (_I, [_P, _I, _I, _U, _P]),
+    "wq_linear_grouped_ex": (_I, [_P, _I, _I, _U, _P]),
     "wq_last_device_status": (_I, []),
     "wq_status_string": (ctypes.c_char_p, [_I]),
     "wq_kernel_launches": (ctypes.c_uint64, []),
@@ -187,6 +199,25 @@ def linear_grouped(problems, fmt, out_f32=False, weights_static=False, stream=No
     flags = (WQ_FLAG_OUT_F32 if out_f32 else 0) | (WQ_FLAG_WEIGHTS_STATIC if weights_static else 0)
     _check("wq_linear_grouped", lib.wq_linear_grouped(ctypes.cast(arr, ctypes.c_void_p), len(problems),
                                                       _fmt(fmt), flags, _stream(stream)))
+
+
+def linear_grouped_ex(problems, fmt, out_f32=False, weights_static=False, stream=None):
+    """Independent Linears of one format in one launch, each writing its output columns to up to
+    WQ_OUT_MAX row-strided destinations.  ``problems`` is a list of (x, packed, scales, N, K, bias,
+    outs) with ``outs`` a list of (view, ncols): ``view`` is a 2-D CUDA tensor view whose first M rows
+    (row stride ``view.stride(0)``) receive the next ``ncols`` output columns."""
+    arr = (wq_problem_ex * len(problems))()
+    for i, (x, packed, scales, N, K, bias, outs) in enumerate(problems):
+        pe = wq_problem_ex()
+        pe.x, pe.packed, pe.scales = x.data_ptr(), packed.data_ptr(), scales.data_ptr()
+        pe.bias = None if bias is None else bias.data_ptr()
+        pe.M, pe.N, pe.K, pe.nout = x.shape[0], N, K, len(outs)
+        for d, (view, ncols) in enumerate(outs):
+            pe.out[d] = wq_out(view.data_ptr(), view.stride(0), ncols)
+        arr[i] = pe
+    flags = (WQ_FLAG_OUT_F32 if out_f32 else 0) | (WQ_FLAG_WEIGHTS_STATIC if weights_static else 0)
+    _check("wq_linear_grouped_ex", lib.wq_linear_grouped_ex(ctypes.cast(arr, ctypes.c_void_p), len(problems),
+                                                            _fmt(fmt), flags, _stream(stream)))
 
 
 def last_device_status():

@@ -201,6 +201,46 @@ typedef struct wq_problem {
 
 int wq_linear_grouped(const wq_problem* problems, int count, int fmt, unsigned flags, void* stream);
 
+/* ---------------------------------------------------------------- grouped, strided outputs
+ * wq_linear_grouped_ex: as wq_linear_grouped, but each problem's output columns
+ * go to up to WQ_OUT_MAX row-strided destinations instead of one dense y.  This
+ * is the fused Q/K/V projection of PR "Run quantized Whisper on the fused Metal
+ * decode path", "Summary" and "Test plan": the projections of a token are
+ * computed in one launch, the bias added on the device, and K and V written
+ * straight into their rows of a KV-cache slab, with no copy afterwards.  It
+ * also serves a merged weight: the cross-attention K and V weights stacked as
+ * one [2N, K] matrix (packed once), whose first N output columns go to the K
+ * slab and the last N to the V slab.
+ *
+ * Destination d of a problem receives the output columns
+ * [c_d, c_d + out[d].ncols), c_d = out[0].ncols + ... + out[d-1].ncols: element
+ * (m, n) is written to out[d].y + m * out[d].ld + (n - c_d) (elements of bf16, or
+ * fp32 with WQ_FLAG_OUT_F32).  Rules (WQ_ERR_ARG / WQ_ERR_ALIGN otherwise):
+ * 1 <= nout <= WQ_OUT_MAX; the ncols sum to N; every ncols but the last is a
+ * multiple of 16; ld >= ncols and ld * element size is a multiple of 16 bytes;
+ * every y is 16-byte aligned.  Destinations must not overlap each other or any
+ * other problem's.  Nothing outside the addressed elements is written: rows of
+ * a slab other than the M addressed ones, and the columns of a row beyond
+ * ncols, keep their contents.                                                  */
+#define WQ_OUT_MAX 4
+typedef struct wq_out {
+  void* y;         /* first element of the destination (device)   */
+  int64_t ld;      /* row stride in elements                       */
+  int64_t ncols;   /* output columns this destination receives     */
+} wq_out;
+
+typedef struct wq_problem_ex {
+  const void* x;          /* bf16 [M, K]                              */
+  const void* packed;     /* packed weight [N, K]                     */
+  const void* scales;     /* its scales blob                          */
+  const uint16_t* bias;   /* bf16 [N] or NULL                         */
+  int64_t M, N, K;
+  int nout;               /* destinations used, 1 .. WQ_OUT_MAX        */
+  wq_out out[WQ_OUT_MAX];
+} wq_problem_ex;
+
+int wq_linear_grouped_ex(const wq_problem_ex* problems, int count, int fmt, unsigned flags, void* stream);
+
 /* ---------------------------------------------------------------- status
  * wq_last_device_status: synchronises the current device, returns and clears
  * the device-side status word (WQ_OK, or WQ_ERR_TIMEOUT if a kernel abandoned
