@@ -87,8 +87,11 @@ int linear_one(const LinearArgs& a, cudaStream_t s) {
   if (a.fmt == WQ_NVFP4_W4A4) {
     if (dense && linear_w4a4_tc(a, s, &rc)) return rc;
   } else if (a.M <= 16) {
-    if (gemv_eligible(a)) return linear_gemv(a, s);
+    // measured on GB300: the CUDA-core GEMV wins for up to 4 activation rows (1280 x 1280 NF4:
+    // 3.5 us against 5.9 us at M = 1), the tensor-core split-K kernel from 5 rows on
+    if (a.M <= kGemvMaxM && gemv_eligible(a)) return linear_gemv(a, s);
     if (dense && linear_tc(a, s, &rc)) return rc;
+    if (gemv_eligible(a)) return linear_gemv(a, s);
   }
   if (a.fmt != WQ_NVFP4_W4A4 && tcp_eligible(a)) return linear_tcp(&a, 1, s);
   return linear_simt(a, s);

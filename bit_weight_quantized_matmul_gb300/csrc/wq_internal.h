@@ -86,6 +86,7 @@ int linear_simt(const LinearArgs& a, cudaStream_t s);
 int take_status_simt();
 
 // ---- linear: decode-sized single Linear on the CUDA cores (wq_gemv.cu)
+constexpr int kGemvMaxM = 4;  // single Linears with up to this many activation rows take the GEMV
 bool gemv_eligible(const LinearArgs& a);
 int linear_gemv(const LinearArgs& a, cudaStream_t s);
 

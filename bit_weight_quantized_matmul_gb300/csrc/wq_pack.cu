@@ -260,13 +260,15 @@ __global__ void nvfp4_quant_kernel(const T* __restrict__ X, int64_t nblk, const 
   }
 #pragma unroll
   for (int i = 0; i < kNVBlock; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const uint32_t s = f32_to_e4m3_satfinite(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
+  const uint32_t s = f32_to_e4m3_cvt(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
   const float S = __fmul_rn(e4m3_to_f32(s), g);
   uint32_t lo = 0, hi = 0;
+  if (S != 0.0f) {  // a block whose scale underflows to zero keeps codes 0
+    float q[kNVBlock];
 #pragma unroll
-  for (int i = 0; i < kNVBlock; ++i) {
-    const uint32_t c = (S == 0.0f) ? 0u : f32_to_e2m1(__fdiv_rn(v[i], S));
-    if (i < 8) lo |= c << (4 * i); else hi |= c << (4 * (i - 8));
+    for (int i = 0; i < kNVBlock; ++i) q[i] = __fdiv_rn(v[i], S);
+    lo = f32x8_to_e2m1x8(q);
+    hi = f32x8_to_e2m1x8(q + 8);
   }
   reinterpret_cast<uint2*>(codes)[b] = make_uint2(lo, hi);
   sf[b] = (uint8_t)s;

@@ -83,14 +83,20 @@ struct PProblem {
   PLay lay;
 };
 
-// Output element (m, n) of problem pr: its address, given the element size.
+// Where output column n of problem pr goes: the address of its element in row 0 and the row stride
+// (elements of T).
 template <typename T>
-__device__ __forceinline__ T* out_ptr(const PProblem& pr, int64_t m, int64_t n) {
+struct OutCol {
+  T* p;
+  int64_t ld;
+};
+template <typename T>
+__device__ __forceinline__ OutCol<T> out_col(const PProblem& pr, int64_t n) {
   int d = 0;
 #pragma unroll
   for (int i = 0; i < WQ_OUT_MAX - 1; ++i) d += (n >= pr.col_end[i]) ? 1 : 0;
   const int64_t c0 = d ? pr.col_end[d - 1] : 0;
-  return reinterpret_cast<T*>(pr.y[d]) + m * pr.ld[d] + (n - c0);
+  return OutCol<T>{reinterpret_cast<T*>(pr.y[d]) + (n - c0), (int64_t)pr.ld[d]};
 }
 
 // Store one 16-column slab of a D tile (TMEM lanes = 128 weight rows n0.., columns = 16 activation
@@ -108,7 +114,8 @@ __device__ __forceinline__ void store_slab_dest(const float (&acc)[16], float gs
   const int row = r >> 3, seg = (r & 7) * 16;
   const int64_t m = m0 + row, n = n0 + seg;
   if (m < pr.M && n < pr.N) {
-    uint16_t* dst = out_ptr<uint16_t>(pr, m, n);
+    const OutCol<uint16_t> oc = out_col<uint16_t>(pr, n);
+    uint16_t* dst = oc.p + m * oc.ld;
     const uint16_t* src = stage + row * 128 + seg;
     if (n + 16 <= pr.N && ((uintptr_t)dst & 15u) == 0) {
       const uint4* s4 = reinterpret_cast<const uint4*>(src);
@@ -574,15 +581,17 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         if (lane == 0) mbar_arrive(&sempty[sb]);
         if (!ok) break;
         if (row_ok) {
+          const OutCol<float> o32 = out_col<float>(pr, n);
+          const OutCol<__nv_bfloat16> o16 = out_col<__nv_bfloat16>(pr, n);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + j;
             if (m < pr.M) {
               const float val = __fadd_rn(acc[j], bval);
               if (P.out_f32)
-                *out_ptr<float>(pr, m, n) = val;
+                o32.p[(int64_t)m * o32.ld] = val;
               else
-                *out_ptr<__nv_bfloat16>(pr, m, n) = __float2bfloat16_rn(val);
+                o16.p[(int64_t)m * o16.ld] = __float2bfloat16_rn(val);
             }
           }
         }
@@ -600,11 +609,11 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
           store_slab_dest(acc, gsc, bval, r, ystage + ((c0 / 16) & 1) * 16 * kRows, pr, m0 + c0,
                           (int64_t)ic.nt * kRows);
         } else if (row_ok) {
+          const OutCol<float> o32 = out_col<float>(pr, n);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
-            if (m < pr.M)
-              *out_ptr<float>(pr, m, n) = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
+            if (m < pr.M) o32.p[(int64_t)m * o32.ld] = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
           }
         }
       }

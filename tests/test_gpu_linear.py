@@ -9,6 +9,7 @@ import torch
 
 from bit_weight_quantized_matmul_gb300 import workloads as wl
 from oracle import linear as L
+from oracle import formats as F
 from oracle import quant as Q
 from tests.gpu_common import (wq, need_gpu, weight_np, oracle_pack, gpu_pack, with_guard, REL_L2_TOL,
                               MAX_ABS_TOL)
@@ -163,3 +164,35 @@ def test_other_block_types(fmt, M, N, K):
     """q4_1, q5_0 (the other GGUF block types) and FP8 E4M3 weights, decode and encoder sizes."""
     need_gpu()
     run_case(fmt, M, N, K, seed=7 * M + N + K)
+
+
+@pytest.mark.parametrize("path", ["gemv", "grouped_decode", "gemm"])
+def test_fp8_every_code_exact_through_each_path(path):
+    """Every finite E4M3 code (both signs, subnormals included) as a weight, picked out by one-hot
+    activation rows: with a row scale of 1 each output is exactly the decoded weight, so every
+    decode (the CUDA-core GEMV, the tensor-core decode and GEMM tiles) must reproduce the oracle's
+    decoded value bit for bit."""
+    need_gpu()
+    vals = F.e4m3_decode(np.arange(0x7F)).astype(np.float32)          # 0x00 .. 0x7E
+    row = np.concatenate([vals, -vals, np.zeros(2, np.float32)])      # 256 values, amax 448
+    N, K = 256, 256
+    W = np.stack([np.roll(row, n) for n in range(N)]).astype(np.float32)
+    p_ref = oracle_pack("fp8", W)
+    w_hat = Q.DEQUANT["fp8"](p_ref)
+    M = 300 if path == "gemm" else 16
+    ks = (np.arange(M) * 37) % K
+    x = np.zeros((M, K), np.float32)
+    x[np.arange(M), ks] = 1.0
+    xb = wl.to_bf16(x).cuda()
+    packed, scales = gpu_pack("fp8", W)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    if path == "grouped_decode":
+        wq().linear_grouped([(y, xb, packed, scales, N, K, None)], "fp8", out_f32=True)
+    else:
+        wq().linear_into(y, xb, packed, scales, "fp8", N, K, None, out_f32=True)
+    torch.cuda.synchronize()
+    assert wq().last_device_status() == 0
+    want = w_hat[:, ks].T.astype(np.float32)
+    got = y.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32) & 0x7FFFFFFF, want.view(np.uint32) & 0x7FFFFFFF) and \
+        np.array_equal(got, want)
