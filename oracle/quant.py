@@ -324,14 +324,16 @@ def to_blobs(p):
     scales: nf4:   int8 absmax codes [N*K/64] | zero pad to 16 B | fp32 s2 [groups] | fp32 offset
             nvfp4: E4M3 bytes [N, K/16] row-major | zero pad to 16 B | fp32 g
             q4_0 / q8_0 / q5_0: fp16 d [N*K/32] | zero pad to 16 B
-            q4_1:  (fp16 d, fp16 m) pairs [N*K/32] | zero pad to 16 B
+            q4_1:  16 zero bytes (its scales are inside the packed units)
             fp8:   fp32 s [N] | zero pad to 16 B
-    q5_0 packed: per 128 consecutive elements of a row, 64 bytes of low nibbles (element 2j in the
-            low nibble of byte j) then 16 bytes of high bits (bit j of byte i is the fifth bit of
-            element 8i + j of the 128).
+    q5_0 / q4_1 packed: 80-byte units, one per 128 consecutive elements of a row: 64 bytes of
+            (low) nibbles, element 2j in the low nibble of byte j, then 16 bytes of side data --
+            q5_0: the fifth bits (bit j of byte i is the fifth bit of element 8i + j);
+            q4_1: the four blocks' (fp16 d, fp16 m) pairs, GGUF keeping a block's scales
+            beside its codes.
     """
     fmt = p["fmt"]
-    if fmt in ("nf4", "nvfp4", "q4_0", "q4_1"):
+    if fmt in ("nf4", "nvfp4", "q4_0"):
         packed = pack_nibbles(p["codes"]).tobytes()
     elif fmt == "q5_0":
         assert p["K"] % 128 == 0, "q5_0 rows hold whole 128-element units"
@@ -339,6 +341,12 @@ def to_blobs(p):
         lo = pack_nibbles(c & 0xF).reshape(-1, 64)
         hi = np.packbits((c >> 4).astype(np.uint8).reshape(-1, 16, 8), axis=2, bitorder="little").reshape(-1, 16)
         packed = np.concatenate([lo, hi], axis=1).tobytes()
+    elif fmt == "q4_1":
+        assert p["K"] % 128 == 0, "q4_1 rows hold whole 128-element units"
+        c = np.asarray(p["codes"], np.uint8).reshape(-1, 128)
+        lo = pack_nibbles(c).reshape(-1, 64)
+        dm = np.stack([np.asarray(p["d"], np.float16), np.asarray(p["m"], np.float16)], axis=1)
+        packed = np.concatenate([lo, dm.reshape(-1, 8).view(np.uint8)], axis=1).tobytes()
     elif fmt == "q8_0":
         packed = np.asarray(p["codes"], np.int8).tobytes()
     else:  # fp8
@@ -351,8 +359,7 @@ def to_blobs(p):
         s = np.asarray(p["scales"], np.uint8).tobytes()
         scales = s + b"\0" * (_align16(len(s)) - len(s)) + np.float32(p["g"]).tobytes()
     elif fmt == "q4_1":
-        dm = np.stack([np.asarray(p["d"], np.float16), np.asarray(p["m"], np.float16)], axis=1).tobytes()
-        scales = dm + b"\0" * (_align16(len(dm)) - len(dm))
+        scales = b"\0" * 16  # the (d, m) pairs travel inside the packed units
     elif fmt == "fp8":
         sv = np.asarray(p["s"], np.float32).tobytes()
         scales = sv + b"\0" * (_align16(len(sv)) - len(sv))

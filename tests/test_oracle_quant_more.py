@@ -23,7 +23,7 @@ def _hex_bytes(tokens):
 # ------------------------------------------------------------------ q4_1
 def _q4_1_worked():
     g = golden_dict("q4_1_worked.txt")
-    W = np.zeros((1, 64), np.float32)
+    W = np.zeros((1, 128), np.float32)
     W[0, :32] = float(g["rest0"][0][0])
     W[0, 32:] = float(g["rest1"][0][0])
     x0 = [float(v) for v in g["x0"][0]]
@@ -37,15 +37,19 @@ def test_q4_1_hand_worked_example():
     g, W = _q4_1_worked()
     p = Q.q4_1_pack(W)
     dm = [int(h, 16) for h in g["dm"][0]]
-    assert list(p["d"].view(np.uint16)) == [dm[0], dm[2]]
-    assert list(p["m"].view(np.uint16)) == [dm[1], dm[3]]
+    assert list(p["d"].view(np.uint16)) == [dm[0], dm[2], 0, 0]
+    assert list(p["m"].view(np.uint16)) == [dm[1], dm[3], 0, 0]
     c0 = [int(c) for c in g["codes0"][0]]
     c1 = [int(c) for c in g["codes1"][0]]
     assert list(p["codes"][:len(c0)]) == c0 and np.all(p["codes"][len(c0):32] == 3)
-    assert list(p["codes"][32:32 + len(c1)]) == c1 and np.all(p["codes"][32 + len(c1):] == 8)
+    assert list(p["codes"][32:32 + len(c1)]) == c1 and np.all(p["codes"][32 + len(c1):64] == 8)
+    assert np.all(p["codes"][64:] == 0)
     packed, scales = Q.to_blobs(p)
+    assert len(packed) == 80 and scales == b"\0" * 16
     assert packed[:5] == _hex_bytes(g["packed0"][0]) and packed[16:21] == _hex_bytes(g["packed1"][0])
-    assert scales == bytes([0x00, 0x3C, 0x00, 0x00, 0x00, 0x38, 0x00, 0xC4]) + b"\0" * 8
+    # the unit's side data: (d, m) of blocks 0..3 (blocks 2 and 3 of this 128-element row are zero:
+    # d = m = 0)
+    assert packed[64:80] == bytes([0x00, 0x3C, 0x00, 0x00, 0x00, 0x38, 0x00, 0xC4]) + b"\0" * 8
 
 
 def test_q4_1_code_is_the_nearest_level_brute_force():
@@ -60,6 +64,17 @@ def test_q4_1_code_is_the_nearest_level_brute_force():
             t = np.float32(np.float32(b[blk, j] - m) / d)
             cand = sorted(range(16), key=lambda q: (abs(Fraction(float(t)) - q), q % 2))
             assert p["codes"][blk * 32 + j] == cand[0]
+
+
+def test_q4_1_storage_unit_roundtrips():
+    """Unpacking the 80-byte units gives back every code and every block's (d, m)."""
+    p = Q.q4_1_pack(_rng(20).standard_normal((3, 256)).astype(np.float32))
+    packed, _ = Q.to_blobs(p)
+    u = np.frombuffer(packed, np.uint8).reshape(-1, 80)
+    assert np.array_equal(Q.unpack_nibbles(u[:, :64].reshape(-1)).reshape(-1, 128), p["codes"].reshape(-1, 128))
+    dm = u[:, 64:].copy().view(np.float16).reshape(-1, 2)
+    assert np.array_equal(dm[:, 0].view(np.uint16), p["d"].view(np.uint16))
+    assert np.array_equal(dm[:, 1].view(np.uint16), p["m"].view(np.uint16))
 
 
 def test_q4_1_roundtrip_and_extremes():
