@@ -38,7 +38,7 @@ ScalesLayout scales_layout(int fmt, int64_t N, int64_t K) {
       L.total = align16((size_t)(n / 32) * 2);
       break;
     case WQ_Q4_1:
-      L.total = align16((size_t)(n / 32) * 4);
+      L.total = 16;  // the (d, m) pairs live in the packed units; 16 zero bytes
       break;
     case WQ_FP8:
       L.total = align16((size_t)N * 4);
@@ -112,8 +112,8 @@ int block_of(int fmt) {
     case WQ_NVFP4_W4A4: return 32;  // 16-blocks; rows of packed codes must stay 16-byte aligned
     case WQ_Q4_0:
     case WQ_Q8_0:
-    case WQ_Q4_1:
     case WQ_FP8: return 32;
+    case WQ_Q4_1:
     case WQ_Q5_0: return 128;  // whole 128-element storage units per row
     default: return 0;
   }

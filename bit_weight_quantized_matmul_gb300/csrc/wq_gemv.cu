@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kWarps * 32) wq_gemv_kernel(GemvParams p) {
   uint4 wv[kR][kPLMax][GFmt<FMT>::PW];
   uint32_t sw[kR][kPLMax];   // raw scale word of each piece (format-specific)
   float s2v[kR][kPLMax];     // NF4: second-level scale of the piece's block
-  uint32_t hb[kR][kPLMax];   // q5_0: the piece's fifth bits
+  uint32_t hb[kR][kPLMax];   // q5_0: the piece's fifth bits; q4_1: its (d, m) pair
 #pragma unroll
   for (int r = 0; r < kR; ++r) {
     const int64_t n = row0 + r;
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kWarps * 32) wq_gemv_kernel(GemvParams p) {
       for (int w = 0; w < GFmt<FMT>::PW; ++w) wv[r][j][w] = make_uint4(0u, 0u, 0u, 0u);
       if (!row_ok || pc >= npieces) continue;
       const int64_t e0 = n * p.K + (int64_t)pc * 32;  // first element of the piece
-      if (FMT == WQ_Q5_0) {
+      if (FMT == WQ_Q5_0 || FMT == WQ_Q4_1) {  // 80-byte unit: nibbles, then side data per block
         const uint8_t* unit = p.packed + (e0 / 128) * 80;
         wv[r][j][0] = ld_stream_v4(unit + (pc & 3) * 16);
         hb[r][j] = __ldg(reinterpret_cast<const uint32_t*>(unit + 64) + (pc & 3));
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kWarps * 32) wq_gemv_kernel(GemvParams p) {
       } else if (FMT == WQ_NVFP4) {
         sw[r][j] = __ldg(reinterpret_cast<const uint16_t*>(p.scales) + e0 / 32);  // two E4M3 bytes
       } else if (FMT == WQ_Q4_1) {
-        sw[r][j] = __ldg(reinterpret_cast<const uint32_t*>(p.scales) + e0 / 32);  // (d, m)
+        // (d, m) read with the codes above
       } else if (FMT == WQ_FP8) {
         if (j == 0) sw[r][0] = __float_as_uint(__ldg(reinterpret_cast<const float*>(p.scales) + n));
       } else {
@@ -182,8 +182,8 @@ __global__ void __launch_bounds__(kWarps * 32) wq_gemv_kernel(GemvParams p) {
           sa = e4m3_to_f32(sw[r][j] & 0xFFu);
           sb = e4m3_to_f32(sw[r][j] >> 8);
         } else if (FMT == WQ_Q4_1) {
-          sa = sb = f16_bits_to_f32(sw[r][j] & 0xFFFFu);
-          madd = f16_bits_to_f32(sw[r][j] >> 16);
+          sa = sb = f16_bits_to_f32(hb[r][j] & 0xFFFFu);
+          madd = f16_bits_to_f32(hb[r][j] >> 16);
         } else {
           sa = sb = f16_bits_to_f32(sw[r][j]);
         }

@@ -24,7 +24,8 @@ inline int64_t packed_row_bytes(int fmt, int64_t K) {
   switch (fmt) {
     case WQ_Q8_0:
     case WQ_FP8: return K;
-    case WQ_Q5_0: return K / 128 * 80;
+    case WQ_Q5_0:
+    case WQ_Q4_1: return K / 128 * 80;
     default: return K / 2;
   }
 }

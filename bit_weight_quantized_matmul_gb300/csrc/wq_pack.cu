@@ -347,12 +347,14 @@ __global__ void q8_0_kernel(const float* __restrict__ W, int64_t nb, int8_t* __r
 }
 
 // q4_1: m = fp16(min), d = fp16((max - min) / 15), q = clamp(rint((x - m) / d), 0, 15) against the
-// stored m and d (q = 0 where d == 0); scales hold (d, m) fp16 pairs.
+// stored m and d (q = 0 where d == 0).  Storage unit of 128 elements: 64 bytes of nibbles, then the
+// four blocks' (d, m) fp16 pairs; block b of a unit owns nibble bytes [16b, 16b + 16) and pair
+// bytes [64 + 4b, 64 + 4b + 4).  The scales blob is 16 zero bytes.
 __global__ void q4_1_kernel(const float* __restrict__ W, int64_t nb, uint8_t* __restrict__ packed,
-                            uint32_t* __restrict__ dm_out) {
+                            uint32_t* __restrict__ scales) {
   const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (b == 0)
-    for (int64_t i = nb; i % 4 != 0; ++i) dm_out[i] = 0u;  // zero the pad to 16 bytes
+    for (int i = 0; i < 4; ++i) scales[i] = 0u;
   if (b >= nb) return;
   const float4* src = reinterpret_cast<const float4*>(W + b * kGGBlock);
   float v[kGGBlock];
@@ -374,8 +376,10 @@ __global__ void q4_1_kernel(const float* __restrict__ W, int64_t nb, uint8_t* __
     if (d != 0.0f) q = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[i], m), d)), 0.0f), 15.0f);
     w[i >> 3] |= ((uint32_t)q) << (4 * (i & 7));
   }
-  reinterpret_cast<uint4*>(packed)[b] = make_uint4(w[0], w[1], w[2], w[3]);
-  dm_out[b] = (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(m16) << 16);
+  uint8_t* unit = packed + (b / 4) * 80;
+  *reinterpret_cast<uint4*>(unit + 16 * (b % 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint32_t*>(unit + 64 + 4 * (b % 4)) =
+      (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(m16) << 16);
 }
 
 // q5_0: d = fp16(extreme / -16), q = clamp(rint(x / d) + 16, 0, 31) (q = 16 where d == 0).  Storage
@@ -471,7 +475,9 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t
       r[j] = __fmul_rn((float)q, d);
     }
   } else {
-    const uint32_t c = reinterpret_cast<const uint32_t*>(packed)[t];
+    const uint32_t c = (fmt == WQ_Q4_1)
+                           ? *reinterpret_cast<const uint32_t*>(packed + (e0 / 128) * 80 + (e0 % 128) / 2)
+                           : reinterpret_cast<const uint32_t*>(packed)[t];
     if (fmt == WQ_NF4) {
       const int64_t b = e0 / kNF4Block;
       const int8_t q = reinterpret_cast<const int8_t*>(scales)[b];
@@ -486,7 +492,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t
 #pragma unroll
       for (int j = 0; j < 8; ++j) r[j] = __fmul_rn(__fmul_rn(kE2M1[(c >> (4 * j)) & 15u], s), g);
     } else if (fmt == WQ_Q4_1) {
-      const uint32_t dm = reinterpret_cast<const uint32_t*>(scales)[e0 / kGGBlock];
+      const uint32_t dm = *reinterpret_cast<const uint32_t*>(packed + (e0 / 128) * 80 + 64 + 4 * ((e0 % 128) / 32));
       const float d = f16_bits_to_f32(dm & 0xFFFFu), m = f16_bits_to_f32(dm >> 16);
 #pragma unroll
       for (int j = 0; j < 8; ++j) r[j] = __fadd_rn(__fmul_rn((float)((c >> (4 * j)) & 15u), d), m);

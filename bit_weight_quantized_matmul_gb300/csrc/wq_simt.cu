@@ -61,7 +61,9 @@ __device__ __forceinline__ void decode8(const SimtParams& p, int64_t n, int64_t 
     for (int j = 0; j < 8; ++j) w[j] = __fmul_rn((float)(int8_t)(((j < 4 ? c.x : c.y) >> (8 * (j & 3))) & 0xFF), d);
     return;
   }
-  const uint32_t c = *reinterpret_cast<const uint32_t*>(p.packed + e0 / 2);
+  const uint32_t c = (p.fmt == WQ_Q4_1)
+                         ? *reinterpret_cast<const uint32_t*>(p.packed + (e0 / 128) * 80 + (e0 % 128) / 2)
+                         : *reinterpret_cast<const uint32_t*>(p.packed + e0 / 2);
   if (p.fmt == WQ_NF4) {
     const int64_t b = e0 / 64;
     const int8_t q = reinterpret_cast<const int8_t*>(p.scales)[b];
@@ -71,7 +73,7 @@ __device__ __forceinline__ void decode8(const SimtParams& p, int64_t n, int64_t 
 #pragma unroll
     for (int j = 0; j < 8; ++j) w[j] = __fmul_rn(kNF4[(c >> (4 * j)) & 15u], a);
   } else if (p.fmt == WQ_Q4_1) {
-    const uint32_t dm = reinterpret_cast<const uint32_t*>(p.scales)[e0 / 32];
+    const uint32_t dm = *reinterpret_cast<const uint32_t*>(p.packed + (e0 / 128) * 80 + 64 + 4 * ((e0 % 128) / 32));
     const float d = f16_bits_to_f32(dm & 0xFFFFu), m = f16_bits_to_f32(dm >> 16);
 #pragma unroll
     for (int j = 0; j < 8; ++j) w[j] = __fadd_rn(__fmul_rn((float)((c >> (4 * j)) & 15u), d), m);

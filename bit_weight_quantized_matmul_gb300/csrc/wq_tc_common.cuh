@@ -12,11 +12,12 @@ constexpr int kRows = 128; // weight rows per tile (the MMA M)
 
 template <int FMT>
 struct Fmt {
-  static constexpr bool BYTE = FMT == WQ_Q8_0 || FMT == WQ_FP8;  // one byte per weight
-  static constexpr int WB = BYTE ? 64 : 32;                        // packed bytes per row per 64 weights
+  static constexpr bool BYTE = FMT == WQ_Q8_0 || FMT == WQ_FP8;   // one byte per weight
+  static constexpr bool UNIT = FMT == WQ_Q5_0 || FMT == WQ_Q4_1;  // 80-byte units of 128 weights
+  static constexpr int WB = BYTE ? 64 : UNIT ? 40 : 32;             // packed bytes per row per 64 weights
   // bytes per row and 64-block of the per-block scales staged for a tile (FP8: none, its one
-  // scale per row is applied in the epilogue)
-  static constexpr int SCB = FMT == WQ_NF4 ? 1 : FMT == WQ_FP8 ? 0 : 4;
+  // scale per row is applied in the epilogue; q4_1: none, its scales travel in the units)
+  static constexpr int SCB = FMT == WQ_NF4 ? 1 : (FMT == WQ_FP8 || FMT == WQ_Q4_1) ? 0 : 4;
 };
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -35,6 +36,8 @@ template <int FMT>
 __device__ __forceinline__ float nibble_value(uint32_t c) {
   if (FMT == WQ_NF4) return kNF4[c];
   if (FMT == WQ_Q4_0) return (float)((int)c - 8);
+  if (FMT == WQ_Q4_1) return (float)c;
+  if (FMT == WQ_Q5_0) return (float)((int)c - 16);  // the fifth bit adds 16 afterwards
   return kE2M1[c];  // NVFP4: E2M1 value; the E4M3 block scale multiplies it, g is applied on D
 }
 
@@ -307,6 +310,50 @@ __device__ __forceinline__ void decode_span_fp8(const uint4* wv, uint32_t (&out)
     for (int j = 0; j < 4; ++j) {
       out[q * 8 + j * 2] = e4m3x2_to_bf16x2(prmt(u[j], 0u, 0x4140u));
       out[q * 8 + j * 2 + 1] = e4m3x2_to_bf16x2(prmt(u[j], 0u, 0x4342u));
+    }
+  }
+}
+}  // namespace tc
+}  // namespace wq
+
+namespace wq {
+namespace tc {
+// q4_1 / q5_0: decode elements [64h, 64h + 64) of a 128-element unit into 32 bf16 pairs: `nib` the
+// 32 bytes of their nibbles, `side` the unit's 8 side-data bytes of its blocks 2h and 2h + 1 (q5_0:
+// fifth bits, bit e = element e of the block; q4_1: the blocks' (fp16 d, fp16 m)), `sword` (q5_0)
+// the two blocks' fp16 d.  The fp32 value is the one wq_dequant gives (q5_0 (q - 16) * d; q4_1
+// q * d + m), rounded once to bf16 for the MMA.
+template <int FMT, int LUTREP>
+__device__ __forceinline__ void decode_unit64(const uint4 (&nib)[2], uint2 side, uint32_t sword, const float2* lut,
+                                              int lsel, uint32_t (&out)[32]) {
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    const uint32_t sd = blk ? side.y : side.x;
+    float d, madd = 0.0f;
+    if (FMT == WQ_Q4_1) {
+      d = f16_bits_to_f32(sd & 0xFFFFu);
+      madd = f16_bits_to_f32(sd >> 16);
+    } else {
+      d = f16_bits_to_f32(blk ? (sword >> 16) : (sword & 0xFFFFu));
+    }
+    const uint4 v = nib[blk];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int e = j * 8 + b * 2;  // element within the block
+        const float2 lv = lut[((u[j] >> (8 * b)) & 0xFFu) * LUTREP + lsel];
+        float v0, v1;
+        if (FMT == WQ_Q5_0) {
+          v0 = __fmul_rn(__fadd_rn(lv.x, ((sd >> e) & 1u) ? 16.0f : 0.0f), d);
+          v1 = __fmul_rn(__fadd_rn(lv.y, ((sd >> (e + 1)) & 1u) ? 16.0f : 0.0f), d);
+        } else {
+          v0 = __fadd_rn(__fmul_rn(lv.x, d), madd);
+          v1 = __fadd_rn(__fmul_rn(lv.y, d), madd);
+        }
+        out[blk * 16 + j * 4 + b] = pack_bf16x2(v0, v1);
+      }
     }
   }
 }

@@ -103,8 +103,10 @@ __device__ __forceinline__ OutCol<T> out_col(const PProblem& pr, int64_t n) {
 // rows m0..) through shared memory: each thread scales and writes its 16 values into stage[m][r],
 // then the threads copy the [16 x 128] bf16 slab out as 16-element runs of one output row with
 // 16-byte stores.  Destination boundaries are multiples of 16 columns, so a run never straddles two.
+// `oc` is the destination of this thread's copy column n0 + (r % 8) * 16, resolved once per tile.
 __device__ __forceinline__ void store_slab_dest(const float (&acc)[16], float gsc, float bval, int r,
-                                                uint16_t* stage, const PProblem& pr, int64_t m0, int64_t n0) {
+                                                uint16_t* stage, const PProblem& pr, const OutCol<uint16_t>& oc,
+                                                int64_t m0, int64_t n0) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float v = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
@@ -114,7 +116,6 @@ __device__ __forceinline__ void store_slab_dest(const float (&acc)[16], float gs
   const int row = r >> 3, seg = (r & 7) * 16;
   const int64_t m = m0 + row, n = n0 + seg;
   if (m < pr.M && n < pr.N) {
-    const OutCol<uint16_t> oc = out_col<uint16_t>(pr, n);
     uint16_t* dst = oc.p + m * oc.ld;
     const uint16_t* src = stage + row * 128 + seg;
     if (n + 16 <= pr.N && ((uintptr_t)dst & 15u) == 0) {
@@ -266,7 +267,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   static_assert(NE == 32 || NE % 64 == 0, "a dequant warp decodes half a 64-block or whole blocks");
   constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
   constexpr int WCHUNK = Fmt<FMT>::WB * SUB;  // packed bytes of one row per chunk
-  constexpr int WRB = WCHUNK < 128 ? WCHUNK : 128;  // row bytes of one W TMA box (swizzle width)
+  // row bytes of one W TMA box: the swizzle width, or (80-byte units) the whole unswizzled chunk
+  constexpr int WRB = Fmt<FMT>::UNIT ? WCHUNK : (WCHUNK < 128 ? WCHUNK : 128);
+  static_assert(!Fmt<FMT>::UNIT || (KC == 128 && MODE == kScaleF32), "unit formats: GEMM tiles of one unit");
   constexpr int WNBOX = WCHUNK / WRB;
 
   extern __shared__ uint8_t smem_raw[];
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
           // the 64-block this warp decodes (NE >= 64), or the block holding its half (NE == 32)
           const int blk = (NE >= 64) ? (KC / 64) * c + NBW * h + bb : (KC / 64) * c + h / 2;
           sword[bb] = 0u;
-          if (!FOLD && FMT != WQ_FP8 && row_ok && blk < nb) {
+          if (!FOLD && Fmt<FMT>::SCB != 0 && row_ok && blk < nb) {
             if (FMT == WQ_NF4) {
               const int8_t qa = (int8_t)sc[r * nb + blk];
               const float s2 = s2s[(n * nb + blk) / 256 - g0];
@@ -488,6 +491,18 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
 #pragma unroll
         for (int bb = 0; bb < NBW; ++bb) {
           uint32_t v[NES / 2];
+          if constexpr (Fmt<FMT>::UNIT) {
+            // one unit per chunk (KC = 128): this warp's 64 elements are nibble bytes [32h, 32h + 32)
+            // and side bytes [64 + 8h, 72 + 8h) of row r's unit
+            static_assert(NES == 64 && NBW == 1, "unit decode");
+            const uint8_t* rowp = wstage + r * WCHUNK;
+            const uint4 nibv[2] = {*reinterpret_cast<const uint4*>(rowp + 32 * h),
+                                   *reinterpret_cast<const uint4*>(rowp + 32 * h + 16)};
+            const uint2 side = *reinterpret_cast<const uint2*>(rowp + 64 + 8 * h);
+            decode_unit64<FMT, LUTREP>(nibv, side, sword[bb], lut, lsel, v);
+            tmem_st_n(tmem_base + lane_base + slot * T::ACOLS + h * (NE / 2) + bb * (NES / 2), v);
+            continue;
+          }
           uint4 wv[CPS];
 #pragma unroll
           for (int k = 0; k < CPS; ++k) wv[k] = load_wchunk<WRB, WNBOX>(wstage, r, ck0 + bb * CPS + k);
@@ -600,16 +615,18 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       if (!mbar_wait(&dfull[buf], (n_it / T::NDB) & 1, abort_flag)) break;
       tc_fence_after();
       uint16_t* ystage = reinterpret_cast<uint16_t*>(smem + S::Y_OFF);
+      const int64_t n_copy = (int64_t)ic.nt * kRows + (r & 7) * 16;  // the column this thread copies out
+      const OutCol<uint16_t> oc16 = out_col<uint16_t>(pr, n_copy < pr.N ? n_copy : 0);
+      const OutCol<float> o32 = out_col<float>(pr, n);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float acc[16];
         tmem_ld16(tmem_base + lane_base + T::D_COL + buf * BN + c0, acc);
         tc_wait_ld();
         if (!P.out_f32) {
-          store_slab_dest(acc, gsc, bval, r, ystage + ((c0 / 16) & 1) * 16 * kRows, pr, m0 + c0,
+          store_slab_dest(acc, gsc, bval, r, ystage + ((c0 / 16) & 1) * 16 * kRows, pr, oc16, m0 + c0,
                           (int64_t)ic.nt * kRows);
         } else if (row_ok) {
-          const OutCol<float> o32 = out_col<float>(pr, n);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
@@ -738,9 +755,10 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
     if (!encode_tmap_2d(&maps.x[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M,
                         (uint64_t)a.K * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
       return WQ_ERR_CUDA;
-    if (!encode_tmap_2d(&maps.w[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, wrow, (uint64_t)a.N, wrow,
-                        std::min(Fmt<FMT>::WB * (KC / 64), 128), kRows,
-                        swizzle_of<std::min(Fmt<FMT>::WB * (KC / 64), 128)>()))
+    constexpr int wbox = Fmt<FMT>::UNIT ? Fmt<FMT>::WB * (KC / 64) : std::min(Fmt<FMT>::WB * (KC / 64), 128);
+    const CUtensorMapSwizzle wswz = Fmt<FMT>::UNIT ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_of<std::min(wbox, 128)>();
+    if (!encode_tmap_2d(&maps.w[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, wrow, (uint64_t)a.N, wrow, wbox, kRows,
+                        wswz))
       return WQ_ERR_CUDA;
   }
   P.total_items = items;
@@ -820,6 +838,16 @@ template <int FMT>
 int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_static, cudaStream_t s) {
   int64_t maxM = 0;
   for (int i = 0; i < count; ++i) maxM = std::max(maxM, probs[i].M);
+  int64_t maxK = 0;
+  for (int i = 0; i < count; ++i) maxK = std::max(maxK, probs[i].K);
+  if constexpr (Fmt<FMT>::UNIT) {
+    // q4_1 / q5_0: encoder-sized GEMM tiles only (tcp_eligible keeps decode-sized problems off
+    // this path); one 128-weight unit per chunk
+    using Wide = PSmem<256, 2, FMT, 128, 1, kScaleF32>;
+    if (maxK <= 64 * Wide::max_blocks())
+      return launch_tcp<256, 2, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
+    return launch_tcp<128, 2, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
+  } else {
   // NVFP4 decodes E2M1 in registers (no table) and scales exactly in bf16
   if (maxM <= 16) {
     constexpr bool reg = FMT == WQ_NVFP4 || FMT == WQ_FP8;  // register decode, exact bf16 scaling
@@ -831,8 +859,6 @@ int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   }
   // GEMM: 256 activation rows per tile (N = 256 MMAs, one TMEM accumulator) where shared memory
   // allows two stages of them and the scale slices of the longest K; else 128 rows (two accumulators)
-  int64_t maxK = 0;
-  for (int i = 0; i < count; ++i) maxK = std::max(maxK, probs[i].K);
   if constexpr (FMT == WQ_NVFP4 || FMT == WQ_FP8) {
     using Wide = PSmem<256, 2, FMT, 128, 0, kScaleBF16>;
     if (maxK <= 64 * Wide::max_blocks())
@@ -851,12 +877,16 @@ int dispatch_p(const LinearArgs* probs, int count, bool out_f32, bool weights_st
   if (maxK <= 64 * Deep::max_blocks())
     return launch_tcp<128, kGemmStagesP, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
   return launch_tcp<128, 2, FMT, 128, 1, kScaleF32>(probs, count, out_f32, weights_static, s);
+  }
 }
 
 }  // namespace
 
 bool tcp_eligible(const LinearArgs& a) {
-  if (a.fmt != WQ_NF4 && a.fmt != WQ_NVFP4 && a.fmt != WQ_Q4_0 && a.fmt != WQ_Q8_0 && a.fmt != WQ_FP8) return false;
+  if (a.fmt != WQ_NF4 && a.fmt != WQ_NVFP4 && a.fmt != WQ_Q4_0 && a.fmt != WQ_Q8_0 && a.fmt != WQ_FP8 &&
+      a.fmt != WQ_Q4_1 && a.fmt != WQ_Q5_0)
+    return false;
+  if ((a.fmt == WQ_Q4_1 || a.fmt == WQ_Q5_0) && a.M <= 16) return false;  // GEMM tiles only
   if (a.K % kKS != 0 || a.K < kKS || a.K > (int64_t)kKS * kMaxChunks) return false;
   if (a.M > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF) return false;
   return ((uintptr_t)a.x & 15u) == 0;
@@ -871,6 +901,8 @@ int linear_tcp(const LinearArgs* probs, int count, cudaStream_t s) {
     case WQ_Q4_0: return dispatch_p<WQ_Q4_0>(probs, count, out_f32, ws, s);
     case WQ_Q8_0: return dispatch_p<WQ_Q8_0>(probs, count, out_f32, ws, s);
     case WQ_FP8: return dispatch_p<WQ_FP8>(probs, count, out_f32, ws, s);
+    case WQ_Q4_1: return dispatch_p<WQ_Q4_1>(probs, count, out_f32, ws, s);
+    case WQ_Q5_0: return dispatch_p<WQ_Q5_0>(probs, count, out_f32, ws, s);
     default: return WQ_ERR_FMT;
   }
 }

@@ -79,17 +79,19 @@ typedef struct wq_act_nvfp4 {
  *   packed  NF4, NVFP4, q4_0, q4_1: N*K/2 bytes, two codes per byte, element
  *           2j of the row-major flattening in the low nibble of byte j.
  *           q8_0: N*K int8.  FP8: N*K E4M3 bytes.
- *           q5_0: N*K*5/8 bytes: per 128 consecutive elements of a row, 64
- *           bytes of low nibbles (element 2j in the low nibble of byte j) then
- *           16 bytes of fifth bits (bit j of byte i = element 8i + j).
+ *           q5_0, q4_1: N*K*5/8 bytes in 80-byte units, one per 128
+ *           consecutive elements of a row: 64 bytes of (low) nibbles, element 2j
+ *           in the low nibble of byte j, then 16 bytes of side data -- q5_0: the
+ *           fifth bits (bit j of byte i = element 8i + j); q4_1: the unit's four
+ *           (fp16 d, fp16 m) pairs, one per 32-block.
  *   scales  NF4:   int8 absmax codes [N*K/64] | zero pad to 16 B |
  *                  fp32 second-level scale s2 [ceil(N*K/64 / 256)] | fp32 offset
  *           NVFP4: E4M3 block scales [N, K/16] row-major | zero pad to 16 B | fp32 g
  *           q4_0, q8_0, q5_0: fp16 d [N*K/32] | zero pad to 16 B
- *           q4_1:  (fp16 d, fp16 m) pairs [N*K/32] | zero pad to 16 B
+ *           q4_1:  16 zero bytes (its scales are inside the packed units)
  *           FP8:   fp32 s [N] | zero pad to 16 B
- * Size rules: NF4 K % 64 == 0; NVFP4 K % 32 == 0; q4_0 / q8_0 / q4_1 / FP8
- * K % 32 == 0; q5_0 K % 128 == 0.                                             */
+ * Size rules: NF4 K % 64 == 0; NVFP4 K % 32 == 0; q4_0 / q8_0 / FP8
+ * K % 32 == 0; q5_0 / q4_1 K % 128 == 0.                                      */
 size_t wq_packed_bytes(int fmt, int64_t N, int64_t K);
 size_t wq_scales_bytes(int fmt, int64_t N, int64_t K);
 

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(wq):
 
 @pytest.mark.parametrize("fmt,N,K", [("nf4", 1536, 384), ("nf4", 3, 6400), ("nf4", 1280, 1280),
                                      ("nvfp4", 1280, 5120), ("nvfp4", 2, 32), ("q4_0", 384, 1536),
-                                     ("q8_0", 5120, 1280), ("q8_0", 1, 32), ("q4_1", 3, 96), ("q4_1", 1280, 1280),
+                                     ("q8_0", 5120, 1280), ("q8_0", 1, 32), ("q4_1", 3, 128), ("q4_1", 1280, 1280),
                                      ("q5_0", 5, 384), ("q5_0", 1280, 5120), ("fp8", 3, 32), ("fp8", 1280, 1280)])
 def test_sizes_match_oracle_blobs(wq, fmt, N, K):
     W = np.random.default_rng(0).standard_normal((N, K)).astype(np.float32) * 0.02

@@ -17,7 +17,7 @@ SHAPES = [
 ]
 
 
-BLOCK = {"nf4": 64, "nvfp4": 32, "q4_0": 32, "q8_0": 32, "q4_1": 32, "q5_0": 128, "fp8": 32}
+BLOCK = {"nf4": 64, "nvfp4": 32, "q4_0": 32, "q8_0": 32, "q4_1": 128, "q5_0": 128, "fp8": 32}
 
 
 @pytest.mark.parametrize("fmt", ["nf4", "nvfp4", "q4_0", "q8_0", "q4_1", "q5_0", "fp8"])
