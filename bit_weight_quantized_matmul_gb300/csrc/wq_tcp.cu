@@ -178,30 +178,18 @@ constexpr int a_slots() { return KC == 256 ? ((MODE == 2 && FMT == WQ_NF4) ? 3 :
 //               warps add  scale * partial  in fp32 -- NF4 / q4_0 / q8_0 decode
 enum { kScaleF32 = 0, kScaleBF16 = 1, kScaleFold = 2 };
 
-// Decode (M <= 16) pipeline depths.  The weight ring is released as soon as the dequant warps have
-// read a tile and the activation ring once the chunk's MMAs completed, so weights can stream
-// ahead of the MMAs; the weight ring takes what shared memory holds next to the scale slices of a
-// K = 5120 tile (1 byte per row and 64-block for NF4, 4 for the others; q8_0 / FP8 tiles are twice
-// as large).
-constexpr int decode_stages(int fmt) {
-  return fmt == WQ_NF4 ? 8 : (fmt == WQ_Q8_0) ? 3 : fmt == WQ_FP8 ? 5 : fmt == WQ_NVFP4 ? 6 : 5;
-}
-constexpr int decode_x_stages(int fmt) { return fmt == WQ_NF4 ? 4 : 3; }
-
 // KC: K elements per pipeline chunk (64 or 128: one or two 128-byte swizzle rows of x)
-// STAGES: weight-tile ring depth; XST: activation-tile ring depth (decode: its own, GEMM: STAGES)
 template <int BN, int STAGES, int FMT, int KC, int LUTREP, int MODE>
 struct PSmem {
-  static constexpr int XST = BN == 16 ? decode_x_stages(FMT) : STAGES;
   static constexpr int SUB = KC / 64;
   static constexpr int XB = SUB * BN * 128;
   static constexpr int WB = kRows * Fmt<FMT>::WB * SUB;
   static constexpr int X_OFF = 0;
-  static constexpr int W_OFF = X_OFF + XST * XB;
+  static constexpr int W_OFF = X_OFF + STAGES * XB;
   static constexpr int LUT_OFF = W_OFF + STAGES * WB;
   static constexpr int LUT_BYTES = (FMT == WQ_Q8_0 || LUTREP == 0) ? 0 : 256 * (MODE == kScaleF32 ? 8 : 4) * LUTREP;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
-  static constexpr int NBAR = 2 * STAGES + 2 * XST + 2 * a_slots<KC, FMT, MODE>() + 9;
+  static constexpr int NBAR = 3 * STAGES + 2 * a_slots<KC, FMT, MODE>() + 9;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;             // [2] 4 KB output slabs
   static constexpr int S2_OFF = Y_OFF + 2 * 16 * kRows * 2;                   // [2][kS2Max] NF4 s2 + offset
@@ -287,9 +275,8 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
-  constexpr int XST = S::XST;
   uint64_t* wfull = bars;           // [STAGES] a stage's weight tile has landed
-  uint64_t* wempty = bars + STAGES; // [STAGES] the dequant warps have read a stage's weight tile
+  uint64_t* empty = bars + STAGES;
   uint64_t* afull = bars + 2 * STAGES;
   uint64_t* aempty = afull + kNA;
   uint64_t* dfull = aempty + kNA;  // [2]
@@ -297,8 +284,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   uint64_t* sfull = dempty + 2;    // [2]
   uint64_t* sempty = sfull + 2;    // [2]
   uint64_t* done = sempty + 2;     // every warp has finished (TMEM may be released)
-  uint64_t* xfull = done + 1;      // [XST] an activation stage's tile has landed
-  uint64_t* xempty = xfull + XST;  // [XST] the MMAs that read an activation stage have completed
+  uint64_t* xfull = done + 1;      // [STAGES] a stage's activation tile has landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
   float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
@@ -314,11 +300,8 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&wfull[i], 1);
-      mbar_init(&wempty[i], kDeqWarps);
-    }
-    for (int i = 0; i < XST; ++i) {
       mbar_init(&xfull[i], 1);
-      mbar_init(&xempty[i], CHUNK_COMMITS);
+      mbar_init(&empty[i], CHUNK_COMMITS + kDeqWarps);
     }
     for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], CHUNK_COMMITS); }
     mbar_init(done, NWARPS);
@@ -349,14 +332,31 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
 
   const int total = P.total_items;
   if (warp == 0) {
-    // ------------------------------------------------ TMA producers: lane 0 weight tiles, lane 1
-    // activation tiles, each on its own ring, so that a weight stage is refilled as soon as the
-    // dequant warps have read it, whatever the MMAs are doing
+    // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      for (int i = 0; i < P.nprob; ++i) prefetch_tmap(&maps.w[i]);
-      // weights stream (and are decoded) before the preceding kernel finishes when the caller
-      // promised they are not written by it; otherwise they wait for it
-      if (!P.weights_static) griddep_wait();
+      for (int i = 0; i < P.nprob; ++i) {
+        prefetch_tmap(&maps.w[i]);
+        prefetch_tmap(&maps.x[i]);
+      }
+      // weights of the first STAGES chunks may stream (and be decoded) before the preceding
+      // kernel finishes; weights and activations have separate barriers, so only the MMAs
+      // wait for the activations
+      int pre = 0;
+      if (P.weights_static) {
+        int g = 0;
+        for (ItemIter ii(P); ii.more() && g < STAGES; ii.next()) {
+          const ItemCoord ic = ii.coord(P);
+          const int nch = (P.prob[ic.p].K + KC - 1) / KC;
+          for (int c = 0; c < nch && g < STAGES; ++c, ++g) {
+            mbar_arrive_expect_tx(&wfull[g], (uint32_t)S::WB);
+            for (int b = 0; b < WNBOX; ++b)
+              tma_load_2d(smem + S::W_OFF + g * S::WB + b * 128 * WRB, &maps.w[ic.p], &wfull[g],
+                          c * WCHUNK + b * WRB, ic.nt * kRows);
+          }
+        }
+        pre = g;
+      }
+      griddep_wait();
       int g = 0;
       bool ok = true;
       for (ItemIter ii(P); ii.more() && ok; ii.next()) {
@@ -364,29 +364,19 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         const int nch = (P.prob[ic.p].K + KC - 1) / KC;
         for (int c = 0; c < nch; ++c, ++g) {
           const int s = g % STAGES;
-          // a per-stage barrier cannot complete twice before this wait
-          if (g >= STAGES && !mbar_wait(&wempty[s], ((g / STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&wfull[s], (uint32_t)S::WB);
-          for (int b = 0; b < WNBOX; ++b)
-            tma_load_2d(smem + S::W_OFF + s * S::WB + b * 128 * WRB, &maps.w[ic.p], &wfull[s],
-                        c * WCHUNK + b * WRB, ic.nt * kRows);
-        }
-      }
-    } else if (lane == 1) {
-      for (int i = 0; i < P.nprob; ++i) prefetch_tmap(&maps.x[i]);
-      griddep_wait();  // x may be written by the preceding kernel
-      int g = 0;
-      bool ok = true;
-      for (ItemIter ii(P); ii.more() && ok; ii.next()) {
-        const ItemCoord ic = ii.coord(P);
-        const int nch = (P.prob[ic.p].K + KC - 1) / KC;
-        for (int c = 0; c < nch; ++c, ++g) {
-          const int xs = g % XST;
-          if (g >= XST && !mbar_wait(&xempty[xs], ((g / XST) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&xfull[xs], (uint32_t)S::XB);
+          if (g >= pre) {
+            // stage s is free once chunk g - STAGES is consumed (x by its MMAs, weights by the
+            // dequant warps); a per-stage barrier cannot complete twice before this wait
+            if (g >= STAGES && !mbar_wait(&empty[s], ((g / STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(&wfull[s], (uint32_t)S::WB);
+            for (int b = 0; b < WNBOX; ++b)
+              tma_load_2d(smem + S::W_OFF + s * S::WB + b * 128 * WRB, &maps.w[ic.p], &wfull[s],
+                          c * WCHUNK + b * WRB, ic.nt * kRows);
+          }
+          mbar_arrive_expect_tx(&xfull[s], (uint32_t)S::XB);
 #pragma unroll
           for (int j = 0; j < SUB; ++j)
-            tma_load_2d(smem + S::X_OFF + xs * S::XB + j * BN * 128, &maps.x[ic.p], &xfull[xs], c * KC + j * 64,
+            tma_load_2d(smem + S::X_OFF + s * S::XB + j * BN * 128, &maps.x[ic.p], &xfull[s], c * KC + j * 64,
                         ic.mt * BN);
         }
       }
@@ -412,17 +402,17 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       const uint32_t d_tmem = tmem_base + T::D_COL + buf * BN;
       for (int c = 0; c < nch; ++c, ++g) {
         if (FOLD && (g & 1) != pair) continue;
-        const int xs = g % XST, slot = g % kNA;
+        const int s = g % STAGES, slot = g % kNA;
         // lane 0: the A slot; lane 1 (fold mode): the partial-tile slot; lane 2: the x tile
-        uint64_t* wb = (lane == 0) ? &afull[slot] : (lane == 1) ? &dempty[g & 1] : &xfull[xs];
-        const uint32_t wp = (lane == 0) ? ((g / kNA) & 1) : (lane == 1) ? (((g >> 1) & 1) ^ 1) : ((g / XST) & 1);
+        uint64_t* wb = (lane == 0) ? &afull[slot] : (lane == 1) ? &dempty[g & 1] : &xfull[s];
+        const uint32_t wp = (lane == 0) ? ((g / kNA) & 1) : (lane == 1) ? (((g >> 1) & 1) ^ 1) : ((g / STAGES) & 1);
         const bool act = (lane == 0) || (FOLD && lane == 1 && g >= 2) || (lane == 2);
         if (!mbar_wait_lanes(wb, wp, act, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
           // descriptors as base + compile-time offsets (the 14-bit address field cannot
           // carry: shared addresses stay below 2^18)
-          const uint64_t xdesc = xdesc0 + (uint64_t)((xs * S::XB) >> 4);
+          const uint64_t xdesc = xdesc0 + (uint64_t)((s * S::XB) >> 4);
           const uint32_t a_tmem = tmem_base + slot * T::ACOLS;
           if (FOLD) {
             constexpr int KPG = (KC / 16) / T::G;  // MMA K steps per scale block
@@ -444,7 +434,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
                           (c | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&aempty[slot]);
-          tc_commit(&xempty[xs]);
+          tc_commit(&empty[s]);
         }
         __syncwarp();
       }
@@ -530,7 +520,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) { mbar_arrive(&afull[slot]); mbar_arrive(&wempty[s]); }
+        if (lane == 0) { mbar_arrive(&afull[slot]); mbar_arrive(&empty[s]); }
       }
       __syncwarp();
       if (!FOLD && lane == 0) mbar_arrive(&sempty[sb]);
@@ -837,7 +827,11 @@ int launch_tcp(const LinearArgs* probs, int count, bool out_f32, bool weights_st
 }
 
 // decode: 256-element chunks, lane-replicated bf16-pair table, block scales folded after the
-// MMA (NVFP4 / FP8: exact bf16 decode); GEMM: 128-element chunks, compact fp32 table
+// MMA (NVFP4: exact bf16 scaling); GEMM: 128-element chunks, compact fp32 table
+// Decode is bound by the weight bytes in flight per SM: as many stages as shared memory holds
+// next to the scale slices of a K = 5120 tile (1 byte per row and 64-block for NF4, 4 for the
+// others; q8_0 stages are twice as large).
+constexpr int decode_stages(int fmt) { return fmt == WQ_NF4 ? 6 : (fmt == WQ_Q8_0 || fmt == WQ_FP8) ? 3 : 4; }
 constexpr int kGemmStagesP = 3;
 
 template <int FMT>
