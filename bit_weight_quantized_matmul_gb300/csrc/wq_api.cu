@@ -87,9 +87,15 @@ int linear_one(const LinearArgs& a, cudaStream_t s) {
   if (a.fmt == WQ_NVFP4_W4A4) {
     if (dense && linear_w4a4_tc(a, s, &rc)) return rc;
   } else if (a.M <= 16) {
-    // measured on GB300: the CUDA-core GEMV wins for up to 4 activation rows (1280 x 1280 NF4:
-    // 3.5 us against 5.9 us at M = 1), the tensor-core split-K kernel from 5 rows on
-    if (a.M <= kGemvMaxM && gemv_eligible(a)) return linear_gemv(a, s);
+    // Measured on GB300 (back-to-back launches, NF4): one activation row runs fastest on the CUDA
+    // cores (1280 x 1280: 3.5 us; 5120 x 1280: 5.0 us), as do up to 4 rows of a narrow or long-K
+    // weight; the persistent tensor-core kernel (whole-K 128-row tiles) takes short-K Linears from
+    // there on (5120 x 1280 at 4 rows: 6.1 against 9.9 us; 1280 x 1280 at 16 rows: 5.6 against
+    // 8.3 us for the cluster split-K kernel, which keeps the long-K ones).
+    const bool tcp_short = a.K <= kTcpDecodeMaxK && tcp_eligible(a);
+    if (gemv_eligible(a) && (a.M == 1 || (a.M <= kGemvMaxM && !(tcp_short && a.N >= 4096))))
+      return linear_gemv(a, s);
+    if (tcp_short) return linear_tcp(&a, 1, s);
     if (dense && linear_tc(a, s, &rc)) return rc;
     if (gemv_eligible(a)) return linear_gemv(a, s);
   }

@@ -88,6 +88,7 @@ int take_status_simt();
 
 // ---- linear: decode-sized single Linear on the CUDA cores (wq_gemv.cu)
 constexpr int kGemvMaxM = 4;  // single Linears with up to this many activation rows take the GEMV
+constexpr int kTcpDecodeMaxK = 2048;  // longer single decode Linears split K over a cluster instead
 bool gemv_eligible(const LinearArgs& a);
 int linear_gemv(const LinearArgs& a, cudaStream_t s);
 
