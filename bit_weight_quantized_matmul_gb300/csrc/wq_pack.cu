@@ -238,62 +238,65 @@ __device__ __forceinline__ float nvfp4_g_from_amax(float amax) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
 }
 
-// kQB consecutive 16-blocks per thread (all loads issued before any is used), per block:
-// s = e4m3((amax_b / 6) / g), S = dec(s) * g, code = e2m1(x / S) (0 where S == 0).  g_src holds amax
-// (g_is_amax) or g itself.
-constexpr int kQB = 4;
+// x / S rounded to nearest even, for the 16 elements of a block sharing one S > 0: Markstein's
+// division (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990; Handbook of Floating-Point Arithmetic, ch. 5): with
+// y = RN(1/S), q = RN(x * y) and the residual r = x - q * S (exact in one FMA), RN(q + r * y) is
+// RN(x / S) while no intermediate leaves the normal range.  One correctly rounded reciprocal per
+// block and a few operations per element instead of a full division each; blocks whose S lies
+// outside [2^-100, 2^100] take the plain division.  Only the E2M1 code of the quotient is used, so
+// quotients past 8 (all saturating) are returned as +-8.
+__device__ __forceinline__ void div_block(const float (&v)[16], float S, float (&q)[16]) {
+  if (S > 7.888609e-31f && S < 1.2676506e30f) {
+    const float y = __frcp_rn(S);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float q0 = __fmul_rn(v[i], y);
+      const float r = __fmaf_rn(-q0, S, v[i]);
+      // the quotient keeps x's sign (a -0 or a negative that rounds to zero stays negative); past
+      // |8| every E2M1 code saturates, which also covers a product that overflowed
+      const float qc = fabsf(q0) > 8.0f ? 8.0f : fabsf(__fmaf_rn(r, y, q0));
+      q[i] = copysignf(qc, v[i]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(v[i], S);
+  }
+}
 
+// one thread per 16-block along a row: s = e4m3((amax_b / 6) / g), S = dec(s) * g,
+// code = e2m1(x / S) (0 where S == 0).  g_src holds amax (g_is_amax) or g itself.
 template <typename T>
 __global__ void nvfp4_quant_kernel(const T* __restrict__ X, int64_t nblk, const float* __restrict__ g_src,
                                    int g_is_amax, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                    float* __restrict__ g_copy_out) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const float gs = *g_src;
   const float g = g_is_amax ? nvfp4_g_from_amax(gs) : gs;
-  if (t == 0 && g_copy_out) *g_copy_out = g;
-  const int64_t b0 = t * kQB;
-  if (b0 >= nblk) return;
-  const int nb = (int)((nblk - b0) < kQB ? (nblk - b0) : kQB);
-  float v[kQB][kNVBlock];
+  if (b == 0 && g_copy_out) *g_copy_out = g;
+  if (b >= nblk) return;
+  float v[kNVBlock];
+  float amax = 0.0f;
+  {
+    float lo[8], hi[8];
+    load8_f32(X, b * kNVBlock, lo);
+    load8_f32(X, b * kNVBlock + 8, hi);
 #pragma unroll
-  for (int q = 0; q < kQB; ++q) {
-    if (q < nb) {
-      float lo[8], hi[8];
-      load8_f32(X, (b0 + q) * kNVBlock, lo);
-      load8_f32(X, (b0 + q) * kNVBlock + 8, hi);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) { v[q][i] = lo[i]; v[q][i + 8] = hi[i]; }
-    }
+    for (int i = 0; i < 8; ++i) { v[i] = lo[i]; v[i + 8] = hi[i]; }
   }
-  uint32_t cw[kQB][2], sw = 0;
 #pragma unroll
-  for (int q = 0; q < kQB; ++q) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kNVBlock; ++i) amax = fmaxf(amax, fabsf(v[q][i]));
-    const uint32_t s = f32_to_e4m3_cvt(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
-    const float S = __fmul_rn(e4m3_to_f32(s), g);
-    cw[q][0] = cw[q][1] = 0u;
-    if (S != 0.0f) {  // a block whose scale underflows to zero keeps codes 0
-      float r[kNVBlock];
-#pragma unroll
-      for (int i = 0; i < kNVBlock; ++i) r[i] = __fdiv_rn(v[q][i], S);
-      cw[q][0] = f32x8_to_e2m1x8(r);
-      cw[q][1] = f32x8_to_e2m1x8(r + 8);
-    }
-    sw |= s << (8 * q);
+  for (int i = 0; i < kNVBlock; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const uint32_t s = f32_to_e4m3_cvt(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
+  const float S = __fmul_rn(e4m3_to_f32(s), g);
+  uint32_t lo = 0, hi = 0;
+  if (S != 0.0f) {  // a block whose scale underflows to zero keeps codes 0
+    float q[kNVBlock];
+    div_block(v, S, q);
+    lo = f32x8_to_e2m1x8(q);
+    hi = f32x8_to_e2m1x8(q + 8);
   }
-  if (nb == kQB) {  // whole groups: 32 bytes of codes and 4 scale bytes, vector stores
-    uint4* cdst = reinterpret_cast<uint4*>(codes + b0 * 8);
-    cdst[0] = make_uint4(cw[0][0], cw[0][1], cw[1][0], cw[1][1]);
-    cdst[1] = make_uint4(cw[2][0], cw[2][1], cw[3][0], cw[3][1]);
-    *reinterpret_cast<uint32_t*>(sf + b0) = sw;
-  } else {
-    for (int q = 0; q < nb; ++q) {
-      reinterpret_cast<uint2*>(codes)[b0 + q] = make_uint2(cw[q][0], cw[q][1]);
-      sf[b0 + q] = (uint8_t)(sw >> (8 * q));
-    }
-  }
+  reinterpret_cast<uint2*>(codes)[b] = make_uint2(lo, hi);
+  sf[b] = (uint8_t)s;
 }
 
 // slot: amax -> g; zero the pad bytes between the block scales and g.
@@ -561,8 +564,7 @@ int pack_nvfp4(const float* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* s
   int g = grid_for(n / 8, 256);
   if (g > 304) g = 304;  // about two blocks per SM, each looping; one atomic per block
   amax_kernel<float><<<g, 256, 0, s>>>(W, n, reinterpret_cast<unsigned*>(slot));
-  nvfp4_quant_kernel<float><<<grid_for((nblk + kQB - 1) / kQB, 256), 256, 0, s>>>(W, nblk, slot, 1, packed, scales,
-                                                                                  nullptr);
+  nvfp4_quant_kernel<float><<<grid_for(nblk, 256), 256, 0, s>>>(W, nblk, slot, 1, packed, scales, nullptr);
   nvfp4_finalize_kernel<<<1, 32, 0, s>>>(slot, scales + lay.sf_bytes, (int)(lay.g_off - lay.sf_bytes));
   count_launch(3);
   return launch_status();
@@ -679,8 +681,7 @@ int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, 
   const int64_t n = M * K, nblk = n / kNVBlock;
   if (n == 0) return WQ_OK;
   if (g_in) {
-    nvfp4_quant_kernel<uint16_t><<<grid_for((nblk + kQB - 1) / kQB, 256), 256, 0, s>>>(x, nblk, g_in, 0, codes,
-                                                                                     scales, g_out);
+    nvfp4_quant_kernel<uint16_t><<<grid_for(nblk, 256), 256, 0, s>>>(x, nblk, g_in, 0, codes, scales, g_out);
     count_launch();
     return launch_status();
   }
@@ -688,8 +689,7 @@ int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, 
   int g = grid_for(n / 8, 256);
   if (g > 304) g = 304;
   amax_kernel<uint16_t><<<g, 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(g_out));
-  nvfp4_quant_kernel<uint16_t><<<grid_for((nblk + kQB - 1) / kQB, 256), 256, 0, s>>>(x, nblk, g_out, 1, codes,
-                                                                                   scales, nullptr);
+  nvfp4_quant_kernel<uint16_t><<<grid_for(nblk, 256), 256, 0, s>>>(x, nblk, g_out, 1, codes, scales, nullptr);
   nvfp4_finalize_kernel<<<1, 32, 0, s>>>(g_out, nullptr, 0);
   count_launch(3);
   return launch_status();

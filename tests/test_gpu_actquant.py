@@ -32,3 +32,28 @@ def test_act_quant_all_zero():
     x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
     codes, scales, g = wq().quant_act_nvfp4(x)
     assert g.item() == 1.0 and int(codes.sum()) == 0 and int(scales.sum()) == 0
+
+
+def test_act_quant_many_scales_and_extremes():
+    """Blocks spread over a wide range of scales (x spanning 2^-40 .. 2^40 across blocks) with a
+    static g that puts some block scales at the bottom of E4M3 and saturates others, every sign of
+    zero, and values that make x / S overflow: codes, scales and g bit-exact with the oracle."""
+    need_gpu()
+    rng = np.random.default_rng(5)
+    M, K = 64, 1024
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= np.exp2(rng.integers(-40, 40, size=(M, K // 16))).astype(np.float32).repeat(16, axis=1)
+    x[0, :16] = -0.0
+    x[1, :16] = 0.0
+    x[2, 3] = 3.0e38
+    x[3, :16] = -1e-30
+    xb = wl.to_bf16(x)
+    xf = wl.bf16_as_f32(xb)
+    for g_in in (np.float32(1e-3), np.float32(7.5), None):
+        ref = Q.quant_act_nvfp4(xf, g_in)
+        gt = None if g_in is None else torch.tensor([g_in], dtype=torch.float32, device="cuda")
+        codes, scales, g = wq().quant_act_nvfp4(xb.cuda(), g_in=gt)
+        torch.cuda.synchronize()
+        assert g.item() == float(ref["g"])
+        assert np.array_equal(scales.cpu().numpy(), ref["scales"])
+        assert np.array_equal(codes.cpu().numpy().reshape(-1), Q.pack_nibbles(ref["codes"]))
