@@ -592,13 +592,13 @@ def extra_lines(args, torch, wq, wl, dev, T, flush, peaks):
     # W4A4 bytes: W codes + scales, x codes + scales, y bf16, bias
     w4_bytes = N * K // 2 + N * K // 16 + M * K // 2 + M * K // 16 + 2 * M * N + 2 * N
     attain = min(fp4, hbm * fl / w4_bytes / 1e3)  # TFLOP/s: min(FP4 peak, HBM x arithmetic intensity)
-    t16 = med_ms(graph_of(lambda: wq.linear_into(y, x, p, s, "nvfp4", N, K, b)))
+    t16 = med_ms(graph_of(lambda: wq.linear_into(y, x, p, s, "nvfp4", N, K, b, weights_static=True)))
     wq.quant_act_nvfp4(x, out=act)
-    t44 = med_ms(graph_of(lambda: wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b)))
+    t44 = med_ms(graph_of(lambda: wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b, weights_static=True)))
     t44q = med_ms(graph_of(lambda: (wq.quant_act_nvfp4(x, out=act),
-                                    wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b))))
+                                    wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b, weights_static=True))))
     t44s = med_ms(graph_of(lambda: (wq.quant_act_nvfp4(x, g_in=g_static, out=act),
-                                    wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b))))
+                                    wq.linear_into(y, act, p, s, "nvfp4_w4a4", N, K, b, weights_static=True))))
     out["encoder_fc1_M6000"] = {
         "workload": "encoder fc1 (N=5120, K=1280) at M=6000 (4 x 1500 frames), NVFP4 weights, L2 flushed",
         "w4a16": {"value": tf(t16), "unit": "TFLOP/s", "ms": round(t16, 4), "frac_of_bf16_peak": round(tf(t16) / pk, 4)},
@@ -640,9 +640,10 @@ def encoder_sweeps(torch, wq, wl, dev, T, flush, pk, fp4, steps=3):
         def launch(c):
             if mode == "w4a4":
                 wq.quant_act_nvfp4(c["x"], out=c["act"])
-                wq.linear_into(c["y"], c["act"], c["p"], c["s"], "nvfp4_w4a4", c["N"], c["K"], c["b"])
+                wq.linear_into(c["y"], c["act"], c["p"], c["s"], "nvfp4_w4a4", c["N"], c["K"], c["b"],
+                               weights_static=True)
             else:
-                wq.linear_into(c["y"], c["x"], c["p"], c["s"], "nvfp4", c["N"], c["K"], c["b"])
+                wq.linear_into(c["y"], c["x"], c["p"], c["s"], "nvfp4", c["N"], c["K"], c["b"], weights_static=True)
         graphs = []
         for c in cases:
             with torch.cuda.stream(T.stream):

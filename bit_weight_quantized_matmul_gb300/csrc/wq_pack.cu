@@ -271,6 +271,9 @@ __global__ void nvfp4_quant_kernel(const T* __restrict__ X, int64_t nblk, const 
                                    int g_is_amax, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                    float* __restrict__ g_copy_out) {
   const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // a consumer launched with programmatic dependent launch (the W4A4 GEMM with static weights) may
+  // start its set-up and weight stream now; it waits for this grid before reading the activations
+  griddep_launch_dependents();
   const float gs = *g_src;
   const float g = g_is_amax ? nvfp4_g_from_amax(gs) : gs;
   if (b == 0 && g_copy_out) *g_copy_out = g;

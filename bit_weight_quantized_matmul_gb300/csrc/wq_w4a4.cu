@@ -76,6 +76,7 @@ struct W4Params {
   void* y;
   int M, N, K;
   int ntiles, mtiles, total_items, out_f32;
+  int weights_static;  // programmatic dependent launch: weight tiles stream before the dependency resolves
   uint32_t g_off;
 };
 
@@ -152,6 +153,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&maps.xc);
       prefetch_tmap(&maps.ws);
       prefetch_tmap(&maps.xs);
+      // weight tiles (codes + block scales) of the first stages do not depend on the preceding
+      // kernel when the caller promised static weights: they stream while it finishes (e.g. while
+      // the activation quantiser runs); the activation tiles wait for it
+      auto load_w = [&](int s, int c, int nt) {
+#pragma unroll
+        for (int b = 0; b < kSub; ++b)  // [128 rows x 128 B] boxes, 128-byte swizzle
+          tma_load_2d(smem + Lay::A_OFF + s * kCodeBytes + b * 16384, &maps.wc, &full[s], c * (kKC / 2) + b * 128,
+                      nt * kRows);
+        tma_load_2d(smem + Lay::SA_OFF + s * kSFBytes, &maps.ws, &full[s], c * (kKC / 16), nt * kRows);
+      };
+      auto load_x = [&](int s, int c, int mt) {
+#pragma unroll
+        for (int b = 0; b < kSub; ++b)
+          tma_load_2d(smem + Lay::B_OFF + s * kCodeBytes + b * 16384, &maps.xc, &full[s], c * (kKC / 2) + b * 128,
+                      mt * kRows);
+        tma_load_2d(smem + Lay::SB_OFF + s * kSFBytes, &maps.xs, &full[s], c * (kKC / 16), mt * kRows);
+      };
+      int pre = 0;
+      if (p.weights_static) {
+        for (int it = blockIdx.x; it < total && pre < kStages; it += gridDim.x)
+          for (int c = 0; c < nch && pre < kStages; ++c, ++pre) {
+            mbar_arrive_expect_tx(&full[pre], STAGE_TX);
+            load_w(pre, c, it % p.ntiles);
+          }
+      }
       griddep_wait();
       int g = 0;
       bool ok = true;
@@ -159,17 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = it % p.ntiles, mt = it / p.ntiles;
         for (int c = 0; c < nch; ++c, ++g) {
           const int s = g % kStages;
-          if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], STAGE_TX);
-#pragma unroll
-          for (int b = 0; b < kSub; ++b) {  // [128 rows x 128 B] boxes, 128-byte swizzle
-            tma_load_2d(smem + Lay::A_OFF + s * kCodeBytes + b * 16384, &maps.wc, &full[s], c * (kKC / 2) + b * 128,
-                        nt * kRows);
-            tma_load_2d(smem + Lay::B_OFF + s * kCodeBytes + b * 16384, &maps.xc, &full[s], c * (kKC / 2) + b * 128,
-                        mt * kRows);
+          if (g >= pre) {
+            if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(&full[s], STAGE_TX);
+            load_w(s, c, nt);
           }
-          tma_load_2d(smem + Lay::SA_OFF + s * kSFBytes, &maps.ws, &full[s], c * (kKC / 16), nt * kRows);
-          tma_load_2d(smem + Lay::SB_OFF + s * kSFBytes, &maps.xs, &full[s], c * (kKC / 16), mt * kRows);
+          load_x(s, c, mt);
         }
       }
     }
@@ -344,6 +365,7 @@ int launch_w4a4(const LinearArgs& a, cudaStream_t s, int* rc) {
   p.mtiles = (int)((a.M + kRows - 1) / kRows);
   p.total_items = p.ntiles * p.mtiles;
   p.out_f32 = a.out_f32 ? 1 : 0;
+  p.weights_static = a.weights_static ? 1 : 0;
   p.g_off = (uint32_t)scales_layout(WQ_NVFP4, a.N, a.K).g_off;
 
   cudaLaunchConfig_t cfg = {};

@@ -196,3 +196,11 @@ def test_fp8_every_code_exact_through_each_path(path):
     got = y.cpu().numpy()
     assert np.array_equal(got.view(np.uint32) & 0x7FFFFFFF, want.view(np.uint32) & 0x7FFFFFFF) and \
         np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 1280, 1280), (1500, 5120, 1280), (130, 1280, 5120)])
+def test_w4a4_static_weights_flag(M, N, K):
+    """W4A4 launched with programmatic dependent launch right after the activation quantiser: its
+    weight tiles stream before the quantiser finishes; the result is the same."""
+    need_gpu()
+    run_case("nvfp4_w4a4", M, N, K, seed=200 + M, outliers=0.001, weights_static=True)
