@@ -892,6 +892,58 @@ def run_reference(args, rank, world):
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------- ncu capture cases
+NCU_CASES = ("decoder_grouped", "linear_m1", "linear_fc2_m16", "w4a16_fc1", "w4a4_fc1")
+
+
+def run_ncu_case(name):
+    """A small launch sequence of one kernel for an ncu capture (profiles/ gives the command): each
+    case runs its launch(es) twice eagerly (the capture skips the first round) and synchronises.
+      decoder_grouped  the 40 NF4 decoder Linears, one grouped launch per M in {1, 4, 16}
+      linear_m1        one 1280 x 1280 NF4 Linear at M = 1 (the CUDA-core GEMV)
+      linear_fc2_m16   one 1280 x 5120 NF4 Linear at M = 16 (the cluster split-K kernel)
+      w4a16_fc1        encoder fc1 (5120 x 1280) at M = 6000, NVFP4 W4A16
+      w4a4_fc1         the same in W4A4: static-g activation quantiser, then the FP4 GEMM"""
+    import torch
+    from bit_weight_quantized_matmul_gb300 import build as B
+    B.build()
+    from bit_weight_quantized_matmul_gb300 import wq
+    from bit_weight_quantized_matmul_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    if name == "decoder_grouped":
+        linears, Ms = decoder_workload()
+        packs = [wq.pack("nf4", torch.from_numpy(wl.weight(l["seed"], l["N"], l["K"])).to(dev)) for l in linears]
+        bs = [wl.bias(l["seed"], l["N"]).to(dev) if l["bias"] else None for l in linears]
+        xs = {M: [wl.activations(l["seed"] * 7 + M, M, l["K"]).to(dev) for l in linears] for M in Ms}
+        ys = {M: [torch.empty((M, l["N"]), dtype=torch.bfloat16, device=dev) for l in linears] for M in Ms}
+        run = lambda: [wq.linear_grouped([(ys[M][i], xs[M][i], packs[i][0], packs[i][1], l["N"], l["K"], bs[i])
+                                          for i, l in enumerate(linears)], "nf4", weights_static=True) for M in Ms]
+    elif name in ("linear_m1", "linear_fc2_m16"):
+        M, N, K = (1, 1280, 1280) if name == "linear_m1" else (16, 1280, 5120)
+        p, sc = wq.pack("nf4", torch.from_numpy(wl.weight(3, N, K)).to(dev))
+        x, b = wl.activations(3, M, K).to(dev), wl.bias(3, N).to(dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        run = lambda: wq.linear_into(y, x, p, sc, "nf4", N, K, b, weights_static=True)
+    else:
+        M, N, K = 6000, 5120, 1280
+        p, sc = wq.pack("nvfp4", torch.from_numpy(wl.weight(101, N, K)).to(dev))
+        x, b = wl.activations(101, M, K, outlier_frac=0.001).to(dev), wl.bias(101, N).to(dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        if name == "w4a16_fc1":
+            run = lambda: wq.linear_into(y, x, p, sc, "nvfp4", N, K, b, weights_static=True)
+        else:
+            g = torch.tensor([float(np.abs(wl.bf16_as_f32(x.cpu())).max()) / 2688.0], dtype=torch.float32,
+                             device=dev)
+            act = wq.quant_act_nvfp4(x, g_in=g)
+            run = lambda: (wq.quant_act_nvfp4(x, g_in=g, out=act),
+                           wq.linear_into(y, act, p, sc, "nvfp4_w4a4", N, K, b, weights_static=True))
+    for _ in range(2):
+        run()
+        torch.cuda.synchronize()
+    assert wq.last_device_status() == 0
+    print(f"ncu case {name}: ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -906,7 +958,11 @@ def main():
     ap.add_argument("--cpu-seconds-one-core", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--workload", default="decoder_nf4", choices=["decoder_nf4", "encoder_w4a16", "encoder_w4a4"])
+    ap.add_argument("--ncu-case", choices=NCU_CASES, help="run one small launch sequence for an ncu capture")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
     args.warmup = max(3, args.warmup)
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
