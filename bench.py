@@ -387,7 +387,8 @@ def run_ours(args, rank, local_rank, world):
     reps = T.each(lambda k: graphs[k % 3].replay(), args.reps)
     per_rep = dist_summary(reps, bytes_per_step, "GB/s")
     window = {"steps": win_steps, "seconds": round(win_ms / 1000, 3),
-              "value": round(bytes_per_step * win_steps / (win_ms * 1e-3) / 1e9, 2), "unit": "GB/s"}
+              "value": round(bytes_per_step * win_steps / (win_ms * 1e-3) / 1e9, 2) if win_ms > 0 else None,
+              "unit": "GB/s"}
     sm = clk.get("sm_mhz")
     if sm:
         clk["time_x_median_mhz"] = round(ms_per_step * sm, 3)
