@@ -202,6 +202,7 @@ __device__ __forceinline__ void load8_f32(const uint16_t* p, int64_t i, float (&
 // amax over n values (n % 8 == 0) -> atomicMax on the bit pattern (non-negative floats order as integers)
 template <typename T>
 __global__ void amax_kernel(const T* __restrict__ X, int64_t n, unsigned* __restrict__ slot) {
+  griddep_launch_dependents();  // the quantiser may start loading its blocks
   float a = 0.0f;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x * 8;
   int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
@@ -274,19 +275,22 @@ __global__ void nvfp4_quant_kernel(const T* __restrict__ X, int64_t nblk, const 
   // a consumer launched with programmatic dependent launch (the W4A4 GEMM with static weights) may
   // start its set-up and weight stream now; it waits for this grid before reading the activations
   griddep_launch_dependents();
-  const float gs = *g_src;
-  const float g = g_is_amax ? nvfp4_g_from_amax(gs) : gs;
-  if (b == 0 && g_copy_out) *g_copy_out = g;
-  if (b >= nblk) return;
+  // dynamic g: this kernel runs right after the amax kernel (programmatic dependent launch); x does
+  // not depend on it, so the block's values are loaded first and the amax read after the wait
   float v[kNVBlock];
-  float amax = 0.0f;
-  {
+  if (b < nblk) {
     float lo[8], hi[8];
     load8_f32(X, b * kNVBlock, lo);
     load8_f32(X, b * kNVBlock + 8, hi);
 #pragma unroll
     for (int i = 0; i < 8; ++i) { v[i] = lo[i]; v[i + 8] = hi[i]; }
   }
+  if (g_is_amax) griddep_wait();
+  const float gs = *g_src;
+  const float g = g_is_amax ? nvfp4_g_from_amax(gs) : gs;
+  if (b == 0 && g_copy_out) *g_copy_out = g;
+  if (b >= nblk) return;
+  float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < kNVBlock; ++i) amax = fmaxf(amax, fabsf(v[i]));
   const uint32_t s = f32_to_e4m3_cvt(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
@@ -304,6 +308,8 @@ __global__ void nvfp4_quant_kernel(const T* __restrict__ X, int64_t nblk, const 
 
 // slot: amax -> g; zero the pad bytes between the block scales and g.
 __global__ void nvfp4_finalize_kernel(float* slot, uint8_t* pad_begin, int pad_len) {
+  griddep_launch_dependents();
+  griddep_wait();  // launched right after the quantiser, which still reads the slot as amax
   if (threadIdx.x == 0) *slot = nvfp4_g_from_amax(*slot);
   if ((int)threadIdx.x < pad_len) pad_begin[threadIdx.x] = 0;
 }
@@ -692,8 +698,23 @@ int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, 
   int g = grid_for(n / 8, 256);
   if (g > 304) g = 304;
   amax_kernel<uint16_t><<<g, 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(g_out));
-  nvfp4_quant_kernel<uint16_t><<<grid_for(nblk, 256), 256, 0, s>>>(x, nblk, g_out, 1, codes, scales, nullptr);
-  nvfp4_finalize_kernel<<<1, 32, 0, s>>>(g_out, nullptr, 0);
+  // the quantiser and the finalisation start while their predecessor finishes (programmatic
+  // dependent launch); each waits for it before reading the amax slot
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid_for(nblk, 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, nvfp4_quant_kernel<uint16_t>, x, nblk, (const float*)g_out, 1, codes, scales,
+                         (float*)nullptr) != cudaSuccess)
+    return WQ_ERR_CUDA;
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  if (cudaLaunchKernelEx(&cfg, nvfp4_finalize_kernel, g_out, (uint8_t*)nullptr, 0) != cudaSuccess) return WQ_ERR_CUDA;
   count_launch(3);
   return launch_status();
 }
