@@ -11,6 +11,8 @@
 // Metal decode path", "Summary" (q4_0 / q8_0 blocks of 32 with an fp16 d).
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "wq_device.cuh"
 #include "wq_internal.h"
 
@@ -685,6 +687,18 @@ int selftest_timeout(uint32_t polls, cudaStream_t s) {
   return launch_status();
 }
 
+static int sm_count() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+  });
+  return n;
+}
+
 int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, uint8_t* codes,
                     uint8_t* scales, float* g_out, cudaStream_t s) {
   const int64_t n = M * K, nblk = n / kNVBlock;
@@ -695,8 +709,9 @@ int quant_act_nvfp4(const uint16_t* x, int64_t M, int64_t K, const float* g_in, 
     return launch_status();
   }
   if (cudaMemsetAsync(g_out, 0, sizeof(float), s) != cudaSuccess) return WQ_ERR_CUDA;
+  // four CTAs per SM, each thread with four 16-byte loads in flight
   int g = grid_for(n / 8, 256);
-  if (g > 304) g = 304;
+  if (g > 4 * sm_count()) g = 4 * sm_count();
   amax_kernel<uint16_t><<<g, 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(g_out));
   // the quantiser and the finalisation start while their predecessor finishes (programmatic
   // dependent launch); each waits for it before reading the amax slot

@@ -1,4 +1,6 @@
 """NVFP4 runtime activation quantiser against the oracle: bit-exact codes, scales and g."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -57,3 +59,46 @@ def test_act_quant_many_scales_and_extremes():
         assert g.item() == float(ref["g"])
         assert np.array_equal(scales.cpu().numpy(), ref["scales"])
         assert np.array_equal(codes.cpu().numpy().reshape(-1), Q.pack_nibbles(ref["codes"]))
+
+
+@pytest.mark.parametrize("static_g", [False, True])
+def test_act_quant_many_chunks_ragged(static_g):
+    """20.5 M values (16001 x 1280, 1,280,080 blocks: many waves of the quantiser's grid, the last
+    one partial, and a grid-stride amax pass of several rounds); bit-exact everywhere."""
+    need_gpu()
+    M, K = 16001, 1280
+    x = wl.activations(103, M, K, outlier_frac=0.001)
+    xf = wl.bf16_as_f32(x)
+    g_in = np.float32(0.0029) if static_g else None
+    ref = Q.quant_act_nvfp4(xf, g_in)
+    gt = torch.tensor([g_in], dtype=torch.float32, device="cuda") if static_g else None
+    codes, scales, g = wq().quant_act_nvfp4(x.cuda(), g_in=gt)
+    torch.cuda.synchronize()
+    assert g.item() == float(ref["g"])
+    assert np.array_equal(scales.cpu().numpy(), ref["scales"])
+    assert np.array_equal(codes.cpu().numpy().reshape(-1), Q.pack_nibbles(ref["codes"]))
+
+
+@functools.lru_cache(maxsize=1)
+def _fc2_b16_activations():
+    x = wl.activations(102, 24000, 5120, outlier_frac=0.001)
+    return x, wl.bf16_as_f32(x)
+
+
+@pytest.mark.parametrize("static_g", [False, True])
+def test_act_quant_full_fc2_b16_sampled_rows(static_g):
+    """The largest encoder activation (M = 24000, K = 5120, 245 MB of bf16): g from the whole
+    tensor's amax, codes and scales bit-exact on sampled rows (first and last included)."""
+    need_gpu()
+    M, K = 24000, 5120
+    x, xf = _fc2_b16_activations()
+    g_in = np.float32(0.0031) if static_g else None
+    gt = torch.tensor([g_in], dtype=torch.float32, device="cuda") if static_g else None
+    codes, scales, g = wq().quant_act_nvfp4(x.cuda(), g_in=gt)
+    torch.cuda.synchronize()
+    g_ref = g_in if static_g else Q.nvfp4_global(np.max(np.abs(xf)))
+    assert g.item() == float(g_ref)
+    rows = np.concatenate([[0, 1, M // 2, M - 2, M - 1], np.random.default_rng(9).integers(0, M, 59)])
+    rc, rs, _ = Q.nvfp4_quantize(xf[rows], g_ref)
+    assert np.array_equal(scales.cpu().numpy()[rows], rs)
+    assert np.array_equal(codes.cpu().numpy()[rows].reshape(-1), Q.pack_nibbles(rc))
