@@ -14,6 +14,7 @@ SHAPES = [
     (1280, 1280), (5120, 1280), (1280, 5120),   # large-v3-turbo Linears
     (3, 6400),                          # 300 NF4 blocks: a ragged double-quant group
     (1, 64), (7, 128), (200, 320),      # small and ragged
+    (1000, 1088),                       # 17000 NF4 blocks: the parallel double-quant with a ragged last group
 ]
 
 
