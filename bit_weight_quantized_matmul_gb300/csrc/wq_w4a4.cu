@@ -15,7 +15,8 @@
 //   warp 0      TMA: W codes [128 x 512], x codes [128 x 512], both tiles' scales
 //   warp 1      TMEM owner, MMA issuer (8 MMAs of K = 64 per 512-element chunk)
 //   warps 2..5  scale warps: chunk scales smem -> TMEM (replicated 32-lane layout)
-//   warps 6..9  epilogue: tcgen05.ld, * g_x * g_w, + bias, store y
+//   warps 6..13 epilogue, two groups of four (columns 0..63 and 64..127 of D): tcgen05.ld,
+//               * g_x * g_w, + bias, store y
 // D is double-buffered in TMEM so an item's epilogue overlaps the next main loop.
 // All waits are bounded.
 #include <cuda.h>
@@ -32,8 +33,8 @@ namespace wq {
 namespace {
 
 constexpr int kRows = 128;    // weight rows per tile (MMA M) == activation rows per tile (MMA N)
-constexpr int kSFSlots = 4;   // TMEM scale ring
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kEpiGroups = 2;  // groups of four epilogue warps, each draining half of D's columns
 
 // KC: K elements per chunk, 256 or 512 (one or two 128-byte swizzle rows of packed codes)
 template <int KC>
@@ -92,19 +93,20 @@ struct Lay {
   static constexpr int SA_OFF = B_OFF + kStages * kCodeBytes;  // W scales [stage]
   static constexpr int SB_OFF = SA_OFF + kStages * kSFBytes;   // x scales [stage]
   static constexpr int BAR_OFF = SB_OFF + kStages * kSFBytes;
-  static constexpr int NBAR = 2 * kStages + 2 * kSFSlots + 5;
+  static constexpr int NBAR = 3 * kStages + 5;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;  // [2] 4 KB output slabs
+  static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;  // 4 KB output slab per epilogue group
   static constexpr int TOTAL = Y_OFF + 2 * 16 * kRows * 2 + 1024;
   static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
-// TMEM columns: D double buffer [0, 256), scale ring [256, 256 + 4 * 64): per chunk 8 MMAs x
-// (4 columns of weight scales + 4 of activation scales)
+// TMEM columns: D double buffer [0, 256), then one scale slot per shared-memory stage: per chunk
+// KC / 64 MMAs x (4 columns of weight scales + 4 of activation scales)
 constexpr int kDCol = 0;
 constexpr int kSFCol = 2 * kRows;
 constexpr int kTmemCols = 512;
-static_assert(kSFCol + kSFSlots * Geo<512>::kSFCols <= kTmemCols, "TMEM budget");
+static_assert(kSFCol + Geo<512>::kStages * Geo<512>::kSFCols <= kTmemCols, "TMEM budget");
+static_assert(kSFCol + Geo<256>::kStages * Geo<256>::kSFCols <= kTmemCols, "TMEM budget");
 
 template <int KC>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -119,9 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFF);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
-  uint64_t* sffull = bars + 2 * kStages;
-  uint64_t* sfempty = sffull + kSFSlots;
-  uint64_t* dfull = sfempty + kSFSlots;  // [2]
+  uint64_t* sffull = bars + 2 * kStages;  // stage s's scales are in TMEM slot s
+  uint64_t* dfull = sffull + kStages;      // [2]
   uint64_t* dempty = dfull + 2;          // [2]
   uint64_t* done = dempty + 2;           // every warp has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1 + 4); }
     mbar_init(done, kThreads / 32);
-    for (int i = 0; i < kSFSlots; ++i) { mbar_init(&sffull[i], 4); mbar_init(&sfempty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4); }
+    for (int i = 0; i < kStages; ++i) mbar_init(&sffull[i], 4);
+    for (int i = 0; i < 2; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4 * kEpiGroups); }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -197,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------- MMA issuer
     if (lane == 0) {
+      const uint64_t a_desc0 = smem_desc(smem_u32(smem + Lay::A_OFF), 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(smem_u32(smem + Lay::B_OFF), 16, 1024, 2);
       int g = 0, n_it = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++n_it) {
@@ -205,22 +208,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + kDCol + buf * kRows;
         for (int c = 0; c < nch; ++c, ++g) {
-          const int s = g % kStages, slot = g % kSFSlots;
-          // the scale warps waited for stage s's TMA transaction before they filled this slot
-          if (!mbar_wait(&sffull[slot], (g / kSFSlots) & 1, abort_flag)) { ok = false; break; }
+          const int s = g % kStages;
+          // the scale warps waited for stage s's TMA transaction before they filled its scale slot
+          if (!mbar_wait(&sffull[s], (g / kStages) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_s = smem_u32(smem + Lay::A_OFF + s * kCodeBytes);
-          const uint32_t b_s = smem_u32(smem + Lay::B_OFF + s * kCodeBytes);
+          // descriptors differ from stage 0's only in the start-address field (16-byte units)
+          const uint64_t ad = a_desc0 + (uint64_t)((s * kCodeBytes) >> 4);
+          const uint64_t bd = b_desc0 + (uint64_t)((s * kCodeBytes) >> 4);
+          const uint32_t sfa = tmem_base + kSFCol + s * kSFCols;
 #pragma unroll
           for (int i = 0; i < kKC / 64; ++i) {  // K = 64 E2M1 values (32 bytes) per MMA
-            const uint32_t off = (i / 4) * 16384 + (i % 4) * 32;
-            const uint64_t ad = smem_desc(a_s + off, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b_s + off, 16, 1024, 2);
-            const uint32_t sfa = tmem_base + kSFCol + slot * kSFCols + i * 4;
-            const uint32_t sfb = sfa + kSFCols / 2;
-            mma_nvf4_ss(d_tmem, ad, bd, IDESC, sfa, sfb, (c | i) != 0 ? 1u : 0u);
+            constexpr uint32_t kOff16[8] = {0, 2, 4, 6, 1024, 1026, 1028, 1030};  // (i/4)*16384 + (i%4)*32, /16
+            mma_nvf4_ss(d_tmem, ad + kOff16[i], bd + kOff16[i], IDESC, sfa + i * 4, sfa + kSFCols / 2 + i * 4,
+                        (c | i) != 0 ? 1u : 0u);
           }
-          tc_commit(&sfempty[slot]);
+          // one commit frees both the shared-memory stage (with the scale warps' arrivals) and,
+          // through the producer's wait before it refills the stage, the TMEM scale slot
           tc_commit(&empty[s]);
         }
         if (ok) tc_commit(&dfull[buf]);
@@ -239,9 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
       for (int c = 0; c < nch; ++c, ++g) {
-        const int s = g % kStages, slot = g % kSFSlots;
+        // stage s's TMA transaction completing implies that the producer saw the MMAs of chunk
+        // g - kStages finish (it waited for them before refilling the stage): scale slot s is free
+        const int s = g % kStages, slot = s;
         if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag)) { ok = false; break; }
-        if (g >= kSFSlots && !mbar_wait(&sfempty[slot], ((g / kSFSlots) & 1) ^ 1, abort_flag)) { ok = false; break; }
 #pragma unroll
         for (int op = 0; op < 2; ++op) {
           const uint8_t* sbase = smem + (op == 0 ? Lay::SA_OFF : Lay::SB_OFF) + s * kSFBytes;
@@ -271,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int grp = (warp - 6) / 4;  // this group's columns: [64 grp, 64 grp + 64)
     griddep_wait();
     const float gw = *reinterpret_cast<const float*>(p.w_scales + p.g_off);
     const float gs = __fmul_rn(*p.g_x, gw);
@@ -284,20 +289,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&dfull[buf], (n_it >> 1) & 1, abort_flag)) break;
       tc_fence_after();
       const int m0 = mt * kRows;
-      uint16_t* ystage = reinterpret_cast<uint16_t*>(smem + Lay::Y_OFF);
+      uint16_t* ystage = reinterpret_cast<uint16_t*>(smem + Lay::Y_OFF) + grp * 16 * kRows;
+      // 32 columns per tensor-memory wait; each 16-column slab goes out through this group's 4 KB
+      // buffer, guarded by the group's own named barrier (ids 1 and 2) on both sides
 #pragma unroll 1
-      for (int c0 = 0; c0 < kRows; c0 += 16) {
-        float acc[16];
-        tmem_ld16(tmem_base + lane_base + kDCol + buf * kRows + c0, acc);
+      for (int c1 = grp * (kRows / kEpiGroups); c1 < (grp + 1) * (kRows / kEpiGroups); c1 += 32) {
+        float acc[2][16];
+        tmem_ld16(tmem_base + lane_base + kDCol + buf * kRows + c1, acc[0]);
+        tmem_ld16(tmem_base + lane_base + kDCol + buf * kRows + c1 + 16, acc[1]);
         tc_wait_ld();
-        if (!p.out_f32) {
-          tc::store_slab_bf16(acc, gs, bval, r, ystage + ((c0 / 16) & 1) * 16 * kRows, p.y, p.M, p.N, m0 + c0,
-                              (int64_t)nt * kRows);
-        } else if (row_ok) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = m0 + c0 + j;
-            if (m < p.M) reinterpret_cast<float*>(p.y)[(int64_t)m * p.N + n] = __fadd_rn(__fmul_rn(acc[j], gs), bval);
+        for (int h = 0; h < 2; ++h) {
+          const int c0 = c1 + 16 * h;
+          if (!p.out_f32) {
+            tc::epi_bar_id(1 + grp);  // the previous slab has left the buffer
+            tc::store_slab_bf16(acc[h], gs, bval, r, ystage, p.y, p.M, p.N, m0 + c0, (int64_t)nt * kRows, 1 + grp);
+          } else if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int m = m0 + c0 + j;
+              if (m < p.M)
+                reinterpret_cast<float*>(p.y)[(int64_t)m * p.N + n] = __fadd_rn(__fmul_rn(acc[h][j], gs), bval);
+            }
           }
         }
       }
