@@ -255,8 +255,6 @@ __device__ __forceinline__ void decode_span_nvfp4_reg(uint32_t sword, int part, 
 namespace wq {
 namespace tc {
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-// the same barrier for one of several groups of 128 epilogue threads (named barrier `id`)
-__device__ __forceinline__ void epi_bar_id(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
 // Store one 16-column slab of a D tile (TMEM lanes = 128 weight rows n0.., columns = 16
 // activation rows m0..) to y[M, N] bf16 through shared memory: each of the 128 epilogue
@@ -265,13 +263,13 @@ __device__ __forceinline__ void epi_bar_id(int id) { asm volatile("bar.sync %0, 
 // `stage` is this slab's 4 KB buffer; callers alternate two buffers (one barrier per slab).
 __device__ __forceinline__ void store_slab_bf16(const float (&acc)[16], float gsc, float bval, int r,
                                                 uint16_t* stage, void* y, int64_t M, int64_t N, int64_t m0,
-                                                int64_t n0, int bar_id = 1) {
+                                                int64_t n0) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float v = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
     stage[j * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   }
-  epi_bar_id(bar_id);
+  epi_bar();
   // thread t copies 16 elements: row t / 8, columns (t % 8) * 16 .. + 15
   const int row = r >> 3, seg = (r & 7) * 16;
   const int64_t m = m0 + row, n = n0 + seg;

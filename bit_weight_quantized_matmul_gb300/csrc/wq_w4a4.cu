@@ -70,6 +70,40 @@ __device__ __forceinline__ void tmem_st_cols<32>(uint32_t taddr, const uint32_t 
       : "memory");
 }
 
+// One 16-column slab of the accumulator out to y through a 4 KB shared-memory buffer, for epilogue
+// group G (128 threads, named barrier 1 + G): as tc::store_slab_bf16, with a barrier per group.
+template <int G>
+__device__ __forceinline__ void group_bar() {
+  asm volatile("bar.sync %0, 128;" ::"n"(1 + G) : "memory");
+}
+template <int G>
+__device__ __forceinline__ void store_slab_group(const float (&acc)[16], float gsc, float bval, int r,
+                                                 uint16_t* stage, void* y, int64_t M, int64_t N, int64_t m0,
+                                                 int64_t n0) {
+  group_bar<G>();  // the group's previous slab has left the buffer
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float v = __fadd_rn(__fmul_rn(acc[j], gsc), bval);
+    stage[j * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  group_bar<G>();
+  // thread t copies 16 elements: row t / 8, columns (t % 8) * 16 .. + 15
+  const int row = r >> 3, seg = (r & 7) * 16;
+  const int64_t m = m0 + row, n = n0 + seg;
+  if (m < M && n < N) {
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(y) + m * N + n;
+    const uint16_t* src = stage + row * 128 + seg;
+    if (n + 16 <= N && (N & 7) == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      d4[0] = s4[0];
+      d4[1] = s4[1];
+    } else {
+      for (int e = 0; e < 16 && n + e < N; ++e) reinterpret_cast<uint16_t*>(dst)[e] = src[e];
+    }
+  }
+}
+
 struct W4Params {
   const uint8_t* w_scales;   // weight scales blob (E4M3 [N, K/16] | pad | g)
   const float* g_x;          // activation global scale (device)
@@ -291,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = mt * kRows;
       uint16_t* ystage = reinterpret_cast<uint16_t*>(smem + Lay::Y_OFF) + grp * 16 * kRows;
       // 32 columns per tensor-memory wait; each 16-column slab goes out through this group's 4 KB
-      // buffer, guarded by the group's own named barrier (ids 1 and 2) on both sides
+      // buffer, guarded by the group's own named barrier (ids 1 and 2)
 #pragma unroll 1
       for (int c1 = grp * (kRows / kEpiGroups); c1 < (grp + 1) * (kRows / kEpiGroups); c1 += 32) {
         float acc[2][16];
@@ -302,8 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 2; ++h) {
           const int c0 = c1 + 16 * h;
           if (!p.out_f32) {
-            tc::epi_bar_id(1 + grp);  // the previous slab has left the buffer
-            tc::store_slab_bf16(acc[h], gs, bval, r, ystage, p.y, p.M, p.N, m0 + c0, (int64_t)nt * kRows, 1 + grp);
+            if (grp == 0)
+              store_slab_group<0>(acc[h], gs, bval, r, ystage, p.y, p.M, p.N, m0 + c0, (int64_t)nt * kRows);
+            else
+              store_slab_group<1>(acc[h], gs, bval, r, ystage, p.y, p.M, p.N, m0 + c0, (int64_t)nt * kRows);
           } else if (row_ok) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
