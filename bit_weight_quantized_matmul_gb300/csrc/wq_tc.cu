@@ -46,6 +46,13 @@ struct TcParams {
   ScalesLayout lay;
 };
 
+// Bounded wait that neither looks at the abort flag nor records a status: used after an abort, for
+// the asynchronous copies and MMAs already issued to finish before the CTA releases its memory.
+__device__ __forceinline__ void wait_quiet(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar, parity); ++i) {
+  }
+}
+
 template <int BN, int STAGES, int FMT>
 struct Smem {
   static constexpr int XB = BN * 128;                 // x stage bytes (BN rows x 64 bf16)
@@ -131,13 +138,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_wait();
       for (int i = 0; i < pre; ++i)
         tma_load_2d(smem + S::X_OFF + i * S::XB, &tmX, &full[i], (kc_begin + i) * kKS, m0);
+      int issued = pre;
       for (int i = pre; i < nchunks; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(&full[s], STAGE_TX);
         tma_load_2d(smem + S::W_OFF + s * S::WB, &tmW, &full[s], (kc_begin + i) * Fmt<FMT>::WB, n0);
         tma_load_2d(smem + S::X_OFF + s * S::XB, &tmX, &full[s], (kc_begin + i) * kKS, m0);
+        issued = i + 1;
       }
+      // stopped by a wait that ran out: let the copies of the stages in flight land before exit
+      if (issued < nchunks)
+        for (int c = issued - STAGES < 0 ? 0 : issued - STAGES; c < issued; ++c)
+          wait_quiet(&full[c % STAGES], (c / STAGES) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -273,14 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();
   }
 
-  // Teardown: an mbarrier counts every warp before warp 1 releases TMEM (bounded, and not cut
-  // short by the abort flag: every other wait is bounded, so every warp arrives).
+  // Teardown: an mbarrier counts every warp; warp 1 then waits for the MMA issuer's commit after its
+  // loop (all of its MMAs finished, also after an abort) and releases TMEM.  Bounded, and not cut
+  // short by the abort flag: every other wait is bounded, so every warp arrives.
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(done);
   if (warp == 1) {
-    for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(done, 0); ++i) {
-    }
+    wait_quiet(done, 0);
+    wait_quiet(dfull, 0);
     tc_fence_after();
     tmem_dealloc(tmem_base, T::ALLOC);
   }

@@ -179,6 +179,13 @@ constexpr int a_slots() { return KC == 256 ? ((MODE == 2 && FMT == WQ_NF4) ? 3 :
 enum { kScaleF32 = 0, kScaleBF16 = 1, kScaleFold = 2 };
 
 // KC: K elements per pipeline chunk (64 or 128: one or two 128-byte swizzle rows of x)
+// Bounded wait that neither looks at the abort flag nor records a status: used after an abort, for
+// the asynchronous copies and MMAs already issued to finish before the CTA releases its memory.
+__device__ __forceinline__ void wait_quiet(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar, parity); ++i) {
+  }
+}
+
 template <int BN, int STAGES, int FMT, int KC, int LUTREP, int MODE>
 struct PSmem {
   static constexpr int SUB = KC / 64;
@@ -189,7 +196,7 @@ struct PSmem {
   static constexpr int LUT_OFF = W_OFF + STAGES * WB;
   static constexpr int LUT_BYTES = (FMT == WQ_Q8_0 || LUTREP == 0) ? 0 : 256 * (MODE == kScaleF32 ? 8 : 4) * LUTREP;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
-  static constexpr int NBAR = 3 * STAGES + 2 * a_slots<KC, FMT, MODE>() + 9;
+  static constexpr int NBAR = 3 * STAGES + 2 * a_slots<KC, FMT, MODE>() + 10;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;             // [2] 4 KB output slabs
   static constexpr int S2_OFF = Y_OFF + 2 * 16 * kRows * 2;                   // [2][kS2Max] NF4 s2 + offset
@@ -285,6 +292,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   uint64_t* sempty = sfull + 2;    // [2]
   uint64_t* done = sempty + 2;     // every warp has finished (TMEM may be released)
   uint64_t* xfull = done + 1;      // [STAGES] a stage's activation tile has landed
+  uint64_t* drain = xfull + STAGES;  // every MMA issuer's last commit: all MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
   float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
@@ -305,6 +313,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
     }
     for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], CHUNK_COMMITS); }
     mbar_init(done, NWARPS);
+    mbar_init(drain, NISSUE);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&dfull[i], 1);   // kScaleFold: a partial-tile slot is full
       mbar_init(&dempty[i], 4);  // kScaleFold: a partial-tile slot was folded
@@ -380,6 +389,12 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
                         ic.mt * BN);
         }
       }
+      // stopped by a wait that ran out: let the copies of the stages in flight land before exit
+      if (!ok)
+        for (int c = g - STAGES < 0 ? 0 : g - STAGES; c < g; ++c) {
+          wait_quiet(&wfull[c % STAGES], (c / STAGES) & 1);
+          wait_quiet(&xfull[c % STAGES], (c / STAGES) & 1);
+        }
     }
   } else if (issuer >= 0) {
     // ------------------------------------------------ MMA issuers (whole warp waits, lane 0 issues)
@@ -441,6 +456,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       if (ok && !FOLD && lane == 0) tc_commit(&dfull[buf]);
       __syncwarp();
     }
+    if (lane == 0) tc_commit(drain);  // tracks every MMA this thread issued, also after an abort
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------ dequant warps: half h of every chunk
     const int q = warp & 3;
@@ -642,12 +658,13 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
     // ------------------------------------------------ scale warp: one item ahead of the dequant warps,
     // one bulk copy of the tile's scale slice (contiguous in the blob) into shared memory
     int n_it = 0;
+    bool ok = true;
     for (ItemIter ii(P); ii.more(); ii.next(), ++n_it) {
       const ItemCoord ic = ii.coord(P);
       const PProblem& pr = P.prob[ic.p];
       const int nb = pr.K / 64;
       const int sb = n_it & 1;
-      if (n_it >= 2 && !mbar_wait(&sempty[sb], ((n_it >> 1) & 1) ^ 1, abort_flag)) break;
+      if (n_it >= 2 && !mbar_wait(&sempty[sb], ((n_it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
       const int64_t n0 = (int64_t)ic.nt * kRows;
       const int rows = (int)((pr.N - n0) < kRows ? (pr.N - n0) : kRows);
       const int row_bytes = Fmt<FMT>::SCB * nb;
@@ -675,6 +692,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         mbar_arrive(&sfull[sb]);
       }
     }
+    // stopped by a wait that ran out: the scale copies of the (at most two) items in flight land
+    if (!ok)
+      for (int it = n_it - 2 < 0 ? 0 : n_it - 2; it < n_it; ++it) wait_quiet(&sfull[it & 1], (it >> 1) & 1);
   }
 
   // Teardown: every warp arrives once its own work is over (its MMAs waited for by the
@@ -686,9 +706,10 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   if (lane == 0) mbar_arrive(done);
   if (warp == 1) {
     // bounded, and not cut short by the abort flag: every other wait is bounded, so every
-    // warp arrives; TMEM is released in any case before the CTA exits
-    for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(done, 0); ++i) {
-    }
+    // warp arrives; the issuers' last commits mean no MMA still uses TMEM; TMEM is released in any
+    // case before the CTA exits
+    wait_quiet(done, 0);
+    wait_quiet(drain, 0);
     tc_fence_after();
     tmem_dealloc(tmem_base, T::ALLOC);
   }

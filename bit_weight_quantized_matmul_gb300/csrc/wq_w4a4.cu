@@ -70,6 +70,13 @@ __device__ __forceinline__ void tmem_st_cols<32>(uint32_t taddr, const uint32_t 
       : "memory");
 }
 
+// Bounded wait that neither looks at the abort flag nor records a status: used after an abort, for
+// the asynchronous copies and MMAs already issued to finish before the CTA releases its memory.
+__device__ __forceinline__ void wait_quiet(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar, parity); ++i) {
+  }
+}
+
 // One 16-column slab of the accumulator out to y through a 4 KB shared-memory buffer, for epilogue
 // group G (128 threads, named barrier 1 + G): as tc::store_slab_bf16, with a barrier per group.
 template <int G>
@@ -127,7 +134,7 @@ struct Lay {
   static constexpr int SA_OFF = B_OFF + kStages * kCodeBytes;  // W scales [stage]
   static constexpr int SB_OFF = SA_OFF + kStages * kSFBytes;   // x scales [stage]
   static constexpr int BAR_OFF = SB_OFF + kStages * kSFBytes;
-  static constexpr int NBAR = 3 * kStages + 5;
+  static constexpr int NBAR = 3 * kStages + 6;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;  // 4 KB output slab per epilogue group
   static constexpr int TOTAL = Y_OFF + 2 * 16 * kRows * 2 + 1024;
@@ -159,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dfull = sffull + kStages;      // [2]
   uint64_t* dempty = dfull + 2;          // [2]
   uint64_t* done = dempty + 2;           // every warp has finished
+  uint64_t* drain = done + 1;            // the MMA issuer's last commit: all of its MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::MISC_OFF + 4);
   const int warp = (int)warp_id(), lane = (int)lane_id();
@@ -166,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1 + 4); }
     mbar_init(done, kThreads / 32);
+    mbar_init(drain, 1);
     for (int i = 0; i < kStages; ++i) mbar_init(&sffull[i], 4);
     for (int i = 0; i < 2; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4 * kEpiGroups); }
     *abort_flag = 0;
@@ -228,6 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_x(s, c, mt);
         }
       }
+      // stopped by a wait that ran out: let the copies of the stages in flight land before exit
+      if (!ok)
+        for (int c = g - kStages < 0 ? 0 : g - kStages; c < g; ++c) wait_quiet(&full[c % kStages], (c / kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------- MMA issuer
@@ -262,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) tc_commit(&dfull[buf]);
       }
+      tc_commit(drain);  // tracks every MMA this thread issued, also when a wait ran out
     }
   } else if (warp < 6) {
     // ---------------------------------------------- scale warps: smem [128 rows x KC/16 B] -> TMEM
@@ -357,14 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // Teardown: an mbarrier counts every warp (a CTA-wide bar.sync after lane-divergent roles is not
-  // relied on), then warp 1 releases TMEM.  The wait is bounded and not cut short by the abort
-  // flag: every other wait is bounded, so every warp arrives.
+  // relied on), then warp 1 waits for the MMA issuer's last commit and releases TMEM.  The waits
+  // are bounded and not cut short by the abort flag: every other wait is bounded, so every warp
+  // arrives.
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(done);
   if (warp == 1) {
-    for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(done, 0); ++i) {
-    }
+    wait_quiet(done, 0);
+    wait_quiet(drain, 0);  // no MMA still reads or writes TMEM
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
