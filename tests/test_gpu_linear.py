@@ -112,8 +112,11 @@ def test_simt_path_matches_oracle(fmt):
     run_case(fmt, 33, 256, 320, seed=4, force_simt=True)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1280, 1280), (16, 5120, 1280), (1500, 1280, 1280), (300, 1280, 5120)])
+@pytest.mark.parametrize("M,N,K", [(1, 1280, 1280), (16, 5120, 1280), (1500, 1280, 1280), (300, 1280, 5120),
+                                   (1100, 200, 768), (1030, 264, 1024), (2048, 128, 256)])
 def test_w4a4(M, N, K):
+    """Decode sizes (CUDA cores) and the FP4 tensor-core GEMM: ragged activation and weight tiles,
+    256- and 512-element chunks, a single chunk."""
     need_gpu()
     run_case("nvfp4_w4a4", M, N, K, seed=100 + M, outliers=0.001)
 
@@ -134,7 +137,7 @@ def test_m_zero_is_noop():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("M,K", [(128, 256), (300, 512), (200, 1280)])
+@pytest.mark.parametrize("M,K", [(128, 256), (300, 512), (200, 1280), (1280, 512), (1100, 1280)])
 def test_w4a4_tensor_path_is_exact_products(M, K):
     """W4A4 on the block-scaled FP4 tensor cores: every product e2m1 * e4m3 * e2m1 * e4m3 is exact
     in fp32, so the fp32 output differs from the fp64 oracle only by the accumulation order and the
