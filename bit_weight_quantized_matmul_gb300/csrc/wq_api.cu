@@ -99,6 +99,7 @@ int linear_one(const LinearArgs& a, cudaStream_t s) {
     if (dense && linear_tc(a, s, &rc)) return rc;
     if (gemv_eligible(a)) return linear_gemv(a, s);
   }
+  if (a.fmt != WQ_NVFP4_W4A4 && dense && linear_w4a16_tc(a, s, &rc)) return rc;
   if (a.fmt != WQ_NVFP4_W4A4 && tcp_eligible(a)) return linear_tcp(&a, 1, s);
   return linear_simt(a, s);
 }
@@ -339,8 +340,8 @@ int wq_selftest_encoders(const float* in, int64_t n, uint8_t* out, void* stream)
 int wq_last_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
   int worst = WQ_OK;
-  const int parts[5] = {take_status_pack(), take_status_simt(), take_status_tc(), take_status_tcp(),
-                        take_status_w4a4()};
+  const int parts[6] = {take_status_pack(), take_status_simt(), take_status_tc(), take_status_tcp(),
+                        take_status_w4a4(), take_status_w4a16()};
   for (int v : parts)
     if (v != WQ_OK) worst = v;
   return worst;

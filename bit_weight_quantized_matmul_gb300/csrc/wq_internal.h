@@ -103,6 +103,9 @@ int linear_tc(const LinearArgs& a, cudaStream_t s, int* rc);
 int take_status_tc();
 int linear_w4a4_tc(const LinearArgs& a, cudaStream_t s, int* rc);
 int take_status_w4a4();
+// NVFP4 W4A16 GEMM with 512-row activation tiles (wq_w4a16.cu); 0 = shape not taken
+int linear_w4a16_tc(const LinearArgs& a, cudaStream_t s, int* rc);
+int take_status_w4a16();
 
 // driver entry point for tensor-map encoding (resolved once through the runtime)
 bool encode_tmap_2d(void* tmap, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,

@@ -207,3 +207,37 @@ def test_w4a4_static_weights_flag(M, N, K):
     weight tiles stream before the quantiser finishes; the result is the same."""
     need_gpu()
     run_case("nvfp4_w4a4", M, N, K, seed=200 + M, outliers=0.001, weights_static=True)
+
+
+WIDE_W4A16 = [(2600, 4000, 320), (1100, 20000, 64), (5000, 2000, 1024), (2600, 20000, 128)]
+
+
+@pytest.mark.parametrize("M,N,K", WIDE_W4A16)
+def test_w4a16_wide_tiles(M, N, K):
+    """NVFP4 W4A16 GEMMs on the kernel that decodes each weight tile into shared memory and
+    double-buffers its 256-row accumulators in TMEM: ragged M and N, one to sixteen 64-element chunks;
+    guard rows, tolerance, and bf16 output = fp32 output rounded once."""
+    need_gpu()
+    run_case("nvfp4", M, N, K, seed=M + N + K)
+
+
+@pytest.mark.parametrize("M,N,K", WIDE_W4A16)
+def test_w4a16_wide_tiles_exact_products(M, N, K):
+    """e2m1 * e4m3 weights are exact in bf16 and bf16 * bf16 products exact in fp32, so the fp32
+    output differs from the fp64 oracle only by the accumulation order, the global-scale product and
+    the bias addition: |err| <= (K + 8) 2^-24 sum |x| |w_hat| + 2^-22 |y|."""
+    need_gpu()
+    W = weight_np(5 + K, N, K)
+    x = wl.activations(5 + M, M, K)
+    b = wl.bias(5 + N, N)
+    p_ref = oracle_pack("nvfp4", W)
+    xf = wl.bf16_as_f32(x).astype(np.float64)
+    w_hat = Q.nvfp4_dequant(p_ref).astype(np.float64)
+    y_ref = xf @ w_hat.T + wl.bf16_as_f32(b).astype(np.float64)
+    packed, scales = gpu_pack("nvfp4", W)
+    y = wq().linear(x.cuda(), packed, scales, "nvfp4", N, K, b.cuda(), out_f32=True)
+    torch.cuda.synchronize()
+    assert wq().last_device_status() == 0
+    got = y.cpu().numpy().astype(np.float64)
+    bound = (K + 8) * 2.0 ** -24 * (np.abs(xf) @ np.abs(w_hat).T) + 2.0 ** -22 * np.abs(y_ref) + 1e-30
+    assert np.all(np.abs(got - y_ref) <= bound), float(np.max(np.abs(got - y_ref) / bound))
