@@ -40,9 +40,13 @@ constexpr int kRows = 128;       // weight rows per tile (MMA M)
 constexpr int kHalf = 256;       // activation rows per MMA (N)
 constexpr int kKC = 64;          // K elements per chunk: one 128-byte row of bf16
 constexpr int kNA = 3;           // decoded weight (A) slots
-constexpr int kDeqWarps = 8;
+constexpr int kDeqWarps = 16;                // four per 32-row quarter, 16 elements of a chunk each
+constexpr int kParts = kDeqWarps / 4;          // parts of a 64-element chunk
+constexpr int kEPT = kKC / kParts;             // elements a dequant thread decodes per chunk
+constexpr int kEpiGroups = 1;                  // groups of four epilogue warps
 constexpr int kEpiWarp0 = 2 + kDeqWarps;
-constexpr int kThreads = (kEpiWarp0 + 8) * 32;
+constexpr int kThreads = (kEpiWarp0 + 4 * kEpiGroups) * 32;
+static_assert(kEPT == 16 || kEPT == 32, "dequant part");
 constexpr int kTmemCols = 512;
 
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kDeqWarps + 1); }
     for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 8); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4 * kEpiGroups); }
     mbar_init(done, kThreads / 32);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -232,39 +236,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kEpiWarp0) {
     // ---------------------------------------------- dequant warps
-    // Warp w decodes rows 32 q + lane (q = (w - 2) % 4) and half h = (w - 2) / 4 of each 64-element
-    // chunk: 16 code bytes and two E4M3 scales, 32 bf16 values = 64 bytes of the row's 128.
-    const int q = (warp - 2) & 3, h = (warp - 2) >> 2;
+    // Warp w decodes rows 32 q + lane (q = (w - 2) % 4) and part pt = (w - 2) / 4 of each 64-element
+    // chunk: kEPT / 2 code bytes and kEPT / 16 E4M3 scales, kEPT bf16 values of the row's 64.
+    const int q = (warp - 2) & 3, pt = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const int nb16 = p.K / 16;
+    constexpr int SPC = kEPT / 16;  // scale bytes per part
     int g = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
       const int nt = it % p.ntiles;
       const int64_t n = (int64_t)nt * kRows + r;
       const bool row_ok = n < p.N;
-      const uint16_t* srow = reinterpret_cast<const uint16_t*>(p.scales + (row_ok ? n : 0) * nb16);
-      uint32_t sc_next = row_ok ? __ldg(srow + h) : 0u;  // chunk 0's two scales of this half
+      const uint8_t* srow = p.scales + (row_ok ? n : 0) * nb16 + pt * SPC;
+      auto scale_bytes = [&](int c) -> uint32_t {  // this part's scales of chunk c
+        if (!row_ok) return 0u;
+        return SPC == 2 ? (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(srow + 4 * c)) : (uint32_t)__ldg(srow + 4 * c);
+      };
+      uint32_t sc_next = scale_bytes(0);
       for (int c = 0; c < nch; ++c, ++g) {
         const int s = g % L::STAGES, slot = g % kNA;
         const uint32_t sc = sc_next;
-        if (c + 1 < nch && row_ok) sc_next = __ldg(srow + 2 * (c + 1) + h);
+        if (c + 1 < nch) sc_next = scale_bytes(c + 1);
         if (!mbar_wait(&full[s], (g / L::STAGES) & 1, abort_flag)) { ok = false; break; }
         if (g >= kNA && !mbar_wait(&aempty[slot], ((g / kNA) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        const uint4 wv = tc::load_wchunk<32, 1>(smem + L::W_OFF + s * L::WB, r, h);
-        const uint32_t s0 = __float_as_uint(e4m3_to_f32(sc & 0xFFu)) >> 16;
-        const uint32_t s1 = __float_as_uint(e4m3_to_f32(sc >> 8)) >> 16;
-        const uint32_t sp[2] = {s0 | (s0 << 16), s1 | (s1 << 16)};
-        const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
+        // this part's code bytes: 16-byte piece (kEPT / 2 bytes) pt * kEPT / 32 of the 32-byte row,
+        // stored with TMA's 32-byte swizzle (address bit 4 ^= bit 7)
+        const int boff = pt * (kEPT / 2);
+        const uint32_t off = (uint32_t)(r * 32 + (boff & ~15)) ^ ((uint32_t)((r >> 2) & 1) << 4);
+        const uint8_t* wsrc = smem + L::W_OFF + s * L::WB + off + (boff & 15);
+        uint32_t u[kEPT / 8];
+        if constexpr (kEPT == 32) {
+          const uint4 wv = *reinterpret_cast<const uint4*>(wsrc);
+          u[0] = wv.x; u[1] = wv.y; u[2] = wv.z; u[3] = wv.w;
+        } else {
+          const uint2 wv = *reinterpret_cast<const uint2*>(wsrc);
+          u[0] = wv.x; u[1] = wv.y;
+        }
+        uint32_t sp[SPC];
+#pragma unroll
+        for (int i = 0; i < SPC; ++i) {
+          const uint32_t sb = __float_as_uint(e4m3_to_f32((sc >> (8 * i)) & 0xFFu)) >> 16;
+          sp[i] = sb | (sb << 16);
+        }
         uint8_t* arow = smem + L::A_OFF + slot * L::AB + r * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // 8 codes -> four bf16 pairs -> one 16-byte chunk
+        for (int j = 0; j < kEPT / 8; ++j) {  // 8 codes -> four bf16 pairs -> one 16-byte chunk
           uint32_t w[4];
           tc::e2m1x8_to_bf16(u[j], w);
           const uint32_t spair = sp[j >> 1];
           const uint4 o = make_uint4(tc::hmul2_bf16(w[0], spair), tc::hmul2_bf16(w[1], spair),
                                      tc::hmul2_bf16(w[2], spair), tc::hmul2_bf16(w[3], spair));
-          const int ck = 4 * h + j;  // 16-byte chunk of the 128-byte row, 128-byte swizzle
+          const int ck = pt * (kEPT / 8) + j;  // 16-byte chunk of the 128-byte row, 128-byte swizzle
           *reinterpret_cast<uint4*>(arow + ((ck ^ (r & 7)) << 4)) = o;
         }
         fence_proxy_async_smem();  // the MMAs read the slot through the async proxy
@@ -278,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int grp = (warp - kEpiWarp0) / 4;  // columns [CPG grp, CPG (grp + 1)) of the tile
-    constexpr int CPG = NH * kHalf / 2;
+    constexpr int CPG = NH * kHalf / kEpiGroups;
     griddep_wait();
     const float gsc = *reinterpret_cast<const float*>(p.scales + p.g_off);
     int n_it = 0;
