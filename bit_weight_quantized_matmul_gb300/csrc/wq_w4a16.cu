@@ -39,7 +39,7 @@ namespace {
 constexpr int kRows = 128;       // weight rows per tile (MMA M)
 constexpr int kHalf = 256;       // activation rows per MMA (N)
 constexpr int kKC = 64;          // K elements per chunk: one 128-byte row of bf16
-constexpr int kNA = 3;           // decoded weight (A) slots
+constexpr int kNA = 4;           // decoded weight (A) slots (fills shared memory: 222 KB)
 constexpr int kDeqWarps = 16;                // four per 32-row quarter, 16 elements of a chunk each
 constexpr int kParts = kDeqWarps / 4;          // parts of a 64-element chunk
 constexpr int kEPT = kKC / kParts;             // elements a dequant thread decodes per chunk
