@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (lane == 0) mbar_arrive(done);
   if (warp == 1) {
     wait_quiet(done, 0);
-    wait_quiet(dfull, 0);
+    if (*abort_flag) wait_quiet(dfull, 0);  // else the epilogue waited for it
     tc_fence_after();
     tmem_dealloc(tmem_base, T::ALLOC);
   }

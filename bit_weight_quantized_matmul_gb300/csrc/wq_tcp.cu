@@ -196,7 +196,7 @@ struct PSmem {
   static constexpr int LUT_OFF = W_OFF + STAGES * WB;
   static constexpr int LUT_BYTES = (FMT == WQ_Q8_0 || LUTREP == 0) ? 0 : 256 * (MODE == kScaleF32 ? 8 : 4) * LUTREP;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
-  static constexpr int NBAR = 3 * STAGES + 2 * a_slots<KC, FMT, MODE>() + 10;
+  static constexpr int NBAR = 3 * STAGES + 2 * a_slots<KC, FMT, MODE>() + 9;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int Y_OFF = (MISC_OFF + 16 + 127) / 128 * 128;             // [2] 4 KB output slabs
   static constexpr int S2_OFF = Y_OFF + 2 * 16 * kRows * 2;                   // [2][kS2Max] NF4 s2 + offset
@@ -292,9 +292,11 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   uint64_t* sempty = sfull + 2;    // [2]
   uint64_t* done = sempty + 2;     // every warp has finished (TMEM may be released)
   uint64_t* xfull = done + 1;      // [STAGES] a stage's activation tile has landed
-  uint64_t* drain = xfull + STAGES;  // every MMA issuer's last commit: all MMAs finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
+  // after an abort, every MMA issuer's last commit (all MMAs finished); in the 16-byte misc block
+  static_assert(S::MISC_OFF % 8 == 0, "mbarrier alignment");
+  uint64_t* drain = reinterpret_cast<uint64_t*>(smem + S::MISC_OFF + 8);
   float2* lut = reinterpret_cast<float2*>(smem + S::LUT_OFF);
   uint32_t* lut32 = reinterpret_cast<uint32_t*>(smem + S::LUT_OFF);
   uint8_t* scbuf = smem + S::SC_OFF;
@@ -456,7 +458,8 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       if (ok && !FOLD && lane == 0) tc_commit(&dfull[buf]);
       __syncwarp();
     }
-    if (lane == 0) tc_commit(drain);  // tracks every MMA this thread issued, also after an abort
+    // after an abort: a commit that tracks every MMA this thread issued, for the teardown's wait
+    if (lane == 0 && (!ok || *abort_flag)) tc_commit(drain);
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------ dequant warps: half h of every chunk
     const int q = warp & 3;
@@ -709,7 +712,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
     // warp arrives; the issuers' last commits mean no MMA still uses TMEM; TMEM is released in any
     // case before the CTA exits
     wait_quiet(done, 0);
-    wait_quiet(drain, 0);
+    if (*abort_flag) wait_quiet(drain, 0);  // else the fold / epilogue warps saw every MMA finish
     tc_fence_after();
     tmem_dealloc(tmem_base, T::ALLOC);
   }

@@ -232,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) tc_commit(&dfull[buf]);
       }
-      tc_commit(drain);  // tracks every MMA this thread issued, also when a wait ran out
+      // after an abort: a commit that tracks every MMA this thread issued, for the teardown's wait
+      if (!ok || *abort_flag) tc_commit(drain);
     }
   } else if (warp < kEpiWarp0) {
     // ---------------------------------------------- dequant warps
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (lane == 0) mbar_arrive(done);
   if (warp == 1) {
     wait_quiet(done, 0);
-    wait_quiet(drain, 0);
+    if (*abort_flag) wait_quiet(drain, 0);  // else the epilogue saw every MMA finish
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
