@@ -10,17 +10,20 @@
 // tcgen05.mma.kind::f16 (bf16 x bf16, fp32 accumulate) and g is applied in the epilogue.
 //
 // A tile of 128 weight rows is decoded into shared memory (the canonical 128-byte-swizzled K-major
-// layout the MMA reads) rather than into TMEM, so TMEM holds only accumulators: two of 256 columns,
-// and a tile's epilogue overlaps the next tile's main loop.  Per K step one N = 256 MMA over a
-// 256-row activation tile.  (Two N = 256 MMAs over a 512-row tile with one 512-column accumulator,
-// decoding each weight tile once per 512 rows, measured slower: no overlap of the epilogue and fewer,
-// larger items.)  Persistent CTA per SM over (weight tile, activation tile) items, warp-specialised:
-//   warp 0       TMA: activation tile [256 x 64], weight codes [128 x 32 B]
+// layout the MMA reads) rather than into TMEM, so TMEM holds only accumulators: two of BM columns,
+// and a tile's epilogue overlaps the next tile's main loop.  Per K step one N = BM MMA over a BM-row
+// activation tile: BM = 256, or 128 where 256-row tiles would leave SMs idle (each weight tile is then
+// decoded once per 128 rows instead of 256).  (Two N = 256 MMAs over a 512-row tile with one
+// 512-column accumulator measured slower: no overlap of the epilogue and fewer, larger items.)
+// Persistent CTA per SM over (weight tile, activation tile) items, warp-specialised:
+//   warp 0       TMA: activation tiles [BM x 64] (a stage is released by the MMAs reading it)
 //   warp 1       TMEM owner, MMA issuer (4 K steps per 64-element chunk)
-//   warps 2..9   dequant: E2M1 -> bf16 x E4M3 block scale, 32 elements of one row per thread,
-//                written swizzled into the shared-memory A ring
-//   warps 10..17 epilogue, two groups of four (128 accumulator columns each): tcgen05.ld, * g,
-//                + bias, bf16 y through a 4 KB staging slab per group
+//   warps 2..17  dequant, two groups of eight taking alternate chunks (two chunks decode at once):
+//                E2M1 -> bf16 x E4M3 block scale, 32 elements of one row per thread, written
+//                swizzled into the shared-memory A ring
+//   warps 18..21 epilogue: tcgen05.ld, * g, + bias, bf16 y through a 4 KB staging slab
+//   warp 22      TMA: weight codes [128 x 32 B] on a ring of their own, released by the dequant
+//                warps, so the decode runs ahead of the MMAs by up to the A ring's depth
 // All waits are bounded; after a wait runs out the roles stop and the issued copies and MMAs are
 // drained before TMEM is released.
 #include <cuda.h>
@@ -37,17 +40,18 @@ namespace wq {
 namespace {
 
 constexpr int kRows = 128;       // weight rows per tile (MMA M)
-constexpr int kHalf = 256;       // activation rows per MMA (N)
 constexpr int kKC = 64;          // K elements per chunk: one 128-byte row of bf16
 constexpr int kNA = 4;           // decoded weight (A) slots (fills shared memory: 222 KB)
-constexpr int kDeqWarps = 16;                // four per 32-row quarter, 16 elements of a chunk each
-constexpr int kParts = kDeqWarps / 4;          // parts of a 64-element chunk
+constexpr int kDeqWarps = 16;                  // two groups of eight, alternate chunks
+constexpr int kDeqGroups = 2;
+constexpr int kGroupWarps = kDeqWarps / kDeqGroups;
+constexpr int kParts = kGroupWarps / 4;        // parts of a 64-element chunk
 constexpr int kEPT = kKC / kParts;             // elements a dequant thread decodes per chunk
 constexpr int kEpiGroups = 1;                  // groups of four epilogue warps
 constexpr int kEpiWarp0 = 2 + kDeqWarps;
-constexpr int kThreads = (kEpiWarp0 + 4 * kEpiGroups) * 32;
+constexpr int kWProdWarp = kEpiWarp0 + 4 * kEpiGroups;  // weight-code TMA
+constexpr int kThreads = (kWProdWarp + 1) * 32;
 static_assert(kEPT == 16 || kEPT == 32, "dequant part");
-constexpr int kTmemCols = 512;
 
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -118,38 +122,41 @@ struct W16Maps {
   CUtensorMap x, w;
 };
 
-// NH: MMAs per K step (activation rows per tile = 256 NH; 1 in use); NDB: accumulators in TMEM (two
-// when one tile's 256 columns leave room for a second, so the epilogue overlaps the next tile)
-template <int NH>
+// BM: activation rows per tile (the MMA's N); two BM-column accumulators in TMEM
+template <int BM>
 struct Lay16 {
-  static constexpr int NDB = NH == 1 ? 2 : 1;
-  static constexpr int STAGES = NH == 1 ? 4 : 2;   // activation / weight-code stages
-  static constexpr int XB = NH * kHalf * 128;      // activation stage bytes
+  static_assert(BM == 256 || BM == 128, "activation tile");
+  static constexpr int NDB = 2;
+  static constexpr int TMEM_COLS = NDB * BM;
+  static constexpr int STAGES = BM == 256 ? 4 : 6;   // activation stages
+  static constexpr int WSTAGES = BM == 256 ? 4 : 8;  // weight-code stages
+  static constexpr int XB = BM * 128;                // activation stage bytes
   static constexpr int WB = kRows * (kKC / 2);     // weight-code stage bytes
   static constexpr int AB = kRows * 128;           // decoded weight slot bytes
   static constexpr int X_OFF = 0;
   static constexpr int A_OFF = X_OFF + STAGES * XB;
   static constexpr int W_OFF = A_OFF + kNA * AB;
-  static constexpr int Y_OFF = W_OFF + STAGES * WB;
+  static constexpr int Y_OFF = W_OFF + WSTAGES * WB;
   static constexpr int BAR_OFF = Y_OFF + 2 * 16 * kRows * 2;
-  static constexpr int NBAR = 2 * STAGES + 2 * kNA + 6;
+  static constexpr int NBAR = 2 * STAGES + 2 * WSTAGES + 2 * kNA + 6;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int TOTAL = MISC_OFF + 16 + 1024;
   static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
-template <int NH>
+template <int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     wq_w4a16_kernel(const __grid_constant__ W16Maps maps, const __grid_constant__ W16Params p) {
-  using L = Lay16<NH>;
-  constexpr uint32_t IDESC = idesc_bf16(kRows, kHalf);
-  constexpr uint32_t STAGE_TX = L::XB + L::WB;
+  using L = Lay16<BM>;
+  constexpr uint32_t IDESC = idesc_bf16(kRows, BM);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* full = bars;                  // [L::STAGES] activation + weight codes landed
-  uint64_t* empty = bars + L::STAGES;       // [L::STAGES] codes decoded and activations read by the MMAs
-  uint64_t* afull = bars + 2 * L::STAGES;   // [kNA] decoded weights written
+  uint64_t* full = bars;                      // [L::STAGES] activation tile landed
+  uint64_t* empty = bars + L::STAGES;         // [L::STAGES] the MMAs reading it finished
+  uint64_t* wfull = bars + 2 * L::STAGES;     // [L::WSTAGES] weight codes landed
+  uint64_t* wempty = wfull + L::WSTAGES;      // [L::WSTAGES] weight codes decoded
+  uint64_t* afull = wempty + L::WSTAGES;      // [kNA] decoded weights written
   uint64_t* aempty = afull + kNA;         // [kNA] the MMAs reading them finished
   uint64_t* dfull = aempty + kNA;         // [2] accumulator complete
   uint64_t* dempty = dfull + 2;           // [2] accumulator read out
@@ -160,15 +167,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = (int)warp_id(), lane = (int)lane_id();
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kDeqWarps + 1); }
-    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], 1); }
+    for (int i = 0; i < L::STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < L::WSTAGES; ++i) { mbar_init(&wfull[i], 1); mbar_init(&wempty[i], kGroupWarps); }
+    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kGroupWarps); mbar_init(&aempty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4 * kEpiGroups); }
     mbar_init(done, kThreads / 32);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, L::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -178,24 +186,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nch = p.K / kKC;
   const int total = p.total_items;
   if (warp == 0) {
-    // ---------------------------------------------- TMA producer
+    // ---------------------------------------------- TMA producer: activations
     if (lane == 0) {
       prefetch_tmap(&maps.x);
-      prefetch_tmap(&maps.w);
       griddep_wait();
       int g = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-        const int nt = it % p.ntiles, mt = it / p.ntiles;
+        const int mt = it / p.ntiles;
         for (int c = 0; c < nch; ++c, ++g) {
           const int s = g % L::STAGES;
           if (g >= L::STAGES && !mbar_wait(&empty[s], ((g / L::STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], STAGE_TX);
-#pragma unroll
-          for (int h = 0; h < NH; ++h)
-            tma_load_2d(smem + L::X_OFF + s * L::XB + h * (kHalf * 128), &maps.x, &full[s], c * kKC,
-                        mt * NH * kHalf + h * kHalf);
-          tma_load_2d(smem + L::W_OFF + s * L::WB, &maps.w, &full[s], c * (kKC / 2), nt * kRows);
+          mbar_arrive_expect_tx(&full[s], L::XB);
+          tma_load_2d(smem + L::X_OFF + s * L::XB, &maps.x, &full[s], c * kKC, mt * BM);
         }
       }
       // stopped by a wait that ran out: let the copies of the stages in flight land before exit
@@ -213,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = n_it % L::NDB;
         if (n_it >= L::NDB && !mbar_wait(&dempty[buf], ((n_it / L::NDB) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * (NH * kHalf);
+        const uint32_t d_tmem = tmem_base + buf * BM;
         for (int c = 0; c < nch; ++c, ++g) {
           const int s = g % L::STAGES, slot = g % kNA;
           if (!mbar_wait(&afull[slot], (g / kNA) & 1, abort_flag)) { ok = false; break; }
@@ -223,10 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t xd = x_desc0 + (uint64_t)((s * L::XB) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kKC / 16; ++kk)  // K = 16 bf16 (32 bytes) per MMA
-#pragma unroll
-            for (int h = 0; h < NH; ++h)
-              mma_bf16_ss(d_tmem + h * kHalf, ad + kk * 2, xd + (uint64_t)(h * (kHalf * 128 / 16) + kk * 2), IDESC,
-                          (c | kk) != 0 ? 1u : 0u);
+            mma_bf16_ss(d_tmem, ad + kk * 2, xd + kk * 2, IDESC, (c | kk) != 0 ? 1u : 0u);
           tc_commit(&aempty[slot]);
           tc_commit(&empty[s]);
         }
@@ -237,15 +237,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kEpiWarp0) {
     // ---------------------------------------------- dequant warps
-    // Warp w decodes rows 32 q + lane (q = (w - 2) % 4) and part pt = (w - 2) / 4 of each 64-element
-    // chunk: kEPT / 2 code bytes and kEPT / 16 E4M3 scales, kEPT bf16 values of the row's 64.
-    const int q = (warp - 2) & 3, pt = (warp - 2) >> 2;
+    // Group dg = (w - 2) / 8 decodes the chunks g with g % 2 == dg (every stage and slot index is even
+    // or odd with g, so each group has its own half of both rings); within it, warp w decodes rows
+    // 32 q + lane (q = (w - 2) % 4) and part pt = ((w - 2) / 4) % 2 of the chunk: kEPT / 2 code bytes
+    // and kEPT / 16 E4M3 scales, kEPT bf16 values of the row's 64.
+    static_assert(kNA % kDeqGroups == 0 && L::WSTAGES % kDeqGroups == 0, "rings split between the groups");
+    const int dw = warp - 2;
+    const int dg = dw / kGroupWarps, q = dw & 3, pt = (dw % kGroupWarps) >> 2;
     const int r = q * 32 + lane;
     const int nb16 = p.K / 16;
     constexpr int SPC = kEPT / 16;  // scale bytes per part
-    int g = 0;
+    int gb = 0;  // running chunk index of the item's first chunk
     bool ok = true;
-    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < total && ok; it += gridDim.x, gb += nch) {
       const int nt = it % p.ntiles;
       const int64_t n = (int64_t)nt * kRows + r;
       const bool row_ok = n < p.N;
@@ -254,18 +258,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!row_ok) return 0u;
         return SPC == 2 ? (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(srow + 4 * c)) : (uint32_t)__ldg(srow + 4 * c);
       };
-      uint32_t sc_next = scale_bytes(0);
-      for (int c = 0; c < nch; ++c, ++g) {
-        const int s = g % L::STAGES, slot = g % kNA;
+      const int c0 = ((gb & 1) == dg) ? 0 : 1;  // this group's first chunk of the item
+      uint32_t sc_next = c0 < nch ? scale_bytes(c0) : 0u;
+      for (int c = c0; c < nch; c += kDeqGroups) {
+        const int g = gb + c;
+        const int ws = g % L::WSTAGES, slot = g % kNA;
         const uint32_t sc = sc_next;
-        if (c + 1 < nch) sc_next = scale_bytes(c + 1);
-        if (!mbar_wait(&full[s], (g / L::STAGES) & 1, abort_flag)) { ok = false; break; }
+        if (c + kDeqGroups < nch) sc_next = scale_bytes(c + kDeqGroups);
+        if (!mbar_wait(&wfull[ws], (g / L::WSTAGES) & 1, abort_flag)) { ok = false; break; }
         if (g >= kNA && !mbar_wait(&aempty[slot], ((g / kNA) & 1) ^ 1, abort_flag)) { ok = false; break; }
         // this part's code bytes: 16-byte piece (kEPT / 2 bytes) pt * kEPT / 32 of the 32-byte row,
         // stored with TMA's 32-byte swizzle (address bit 4 ^= bit 7)
         const int boff = pt * (kEPT / 2);
         const uint32_t off = (uint32_t)(r * 32 + (boff & ~15)) ^ ((uint32_t)((r >> 2) & 1) << 4);
-        const uint8_t* wsrc = smem + L::W_OFF + s * L::WB + off + (boff & 15);
+        const uint8_t* wsrc = smem + L::W_OFF + ws * L::WB + off + (boff & 15);
         uint32_t u[kEPT / 8];
         if constexpr (kEPT == 32) {
           const uint4 wv = *reinterpret_cast<const uint4*>(wsrc);
@@ -293,16 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();  // the MMAs read the slot through the async proxy
         __syncwarp();
-        if (lane == 0) { mbar_arrive(&afull[slot]); mbar_arrive(&empty[s]); }
+        if (lane == 0) { mbar_arrive(&afull[slot]); mbar_arrive(&wempty[ws]); }
       }
     }
-  } else {
+  } else if (warp < kWProdWarp) {
     // ---------------------------------------------- epilogue
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int grp = (warp - kEpiWarp0) / 4;  // columns [CPG grp, CPG (grp + 1)) of the tile
-    constexpr int CPG = NH * kHalf / kEpiGroups;
+    constexpr int CPG = BM / kEpiGroups;
     griddep_wait();
     const float gsc = *reinterpret_cast<const float*>(p.scales + p.g_off);
     int n_it = 0;
@@ -315,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&dfull[buf], (n_it / L::NDB) & 1, abort_flag)) break;
       tc_fence_after();
       {
-        const int64_t m0 = (int64_t)mt * NH * kHalf + grp * CPG;
-        const uint32_t dcol = buf * (NH * kHalf) + grp * CPG;
+        const int64_t m0 = (int64_t)mt * BM + grp * CPG;
+        const uint32_t dcol = buf * BM + grp * CPG;
         uint16_t* ystage = reinterpret_cast<uint16_t*>(smem + L::Y_OFF) + grp * 16 * kRows;
 #pragma unroll 1
         for (int c1 = 0; c1 < CPG; c1 += 32) {
@@ -345,6 +351,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&dempty[buf]);
     }
+  } else {
+    // ---------------------------------------------- TMA producer: weight codes (static under programmatic
+    // dependent launch, so no dependency wait)
+    if (lane == 0) {
+      prefetch_tmap(&maps.w);
+      int g = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const int nt = it % p.ntiles;
+        for (int c = 0; c < nch; ++c, ++g) {
+          const int ws = g % L::WSTAGES;
+          if (g >= L::WSTAGES && !mbar_wait(&wempty[ws], ((g / L::WSTAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&wfull[ws], L::WB);
+          tma_load_2d(smem + L::W_OFF + ws * L::WB, &maps.w, &wfull[ws], c * (kKC / 2), nt * kRows);
+        }
+      }
+      if (!ok)
+        for (int c = g - L::WSTAGES < 0 ? 0 : g - L::WSTAGES; c < g; ++c)
+          wait_quiet(&wfull[c % L::WSTAGES], (c / L::WSTAGES) & 1);
+    }
   }
 
   // Teardown: an mbarrier counts every warp, then warp 1 waits for the MMA issuer's last commit and
@@ -356,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_quiet(done, 0);
     if (*abort_flag) wait_quiet(drain, 0);  // else the epilogue saw every MMA finish
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
 }
 
@@ -371,10 +397,10 @@ int num_sms_w16() {
   return n;
 }
 
-template <int NH>
+template <int BM>
 int launch_w4a16(const LinearArgs& a, cudaStream_t s) {
-  using L = Lay16<NH>;
-  auto kern = wq_w4a16_kernel<NH>;
+  using L = Lay16<BM>;
+  auto kern = wq_w4a16_kernel<BM>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -384,7 +410,7 @@ int launch_w4a16(const LinearArgs& a, cudaStream_t s) {
   alignas(64) W16Maps maps;
   const uint64_t kb = (uint64_t)a.K / 2;
   if (!encode_tmap_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M,
-                      (uint64_t)a.K * 2, kKC, kHalf, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                      (uint64_t)a.K * 2, kKC, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.packed, kb, (uint64_t)a.N, kb, kKC / 2, kRows,
                       CU_TENSOR_MAP_SWIZZLE_32B))
     return WQ_ERR_CUDA;
@@ -396,7 +422,7 @@ int launch_w4a16(const LinearArgs& a, cudaStream_t s) {
   p.N = (int)a.N;
   p.K = (int)a.K;
   p.ntiles = (int)((a.N + kRows - 1) / kRows);
-  p.mtiles = (int)((a.M + NH * kHalf - 1) / (NH * kHalf));
+  p.mtiles = (int)((a.M + BM - 1) / BM);
   p.total_items = p.ntiles * p.mtiles;
   p.out_f32 = a.out_f32 ? 1 : 0;
   p.weights_static = a.weights_static ? 1 : 0;
@@ -422,16 +448,27 @@ int launch_w4a16(const LinearArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// 128-row tiles: at least this many activation rows and items, rows of at most kMaxK128 (else the
+// persistent kernel: 1500 x 1280 x 5120 48.1 against 41.5 us; 1500 x 1280 x 1280 19.4 against 21.0)
+constexpr int64_t kMinM128 = 512;
+constexpr int64_t kMaxK128 = 2048;
+constexpr int64_t kMinItems128 = 96;
+
 int linear_w4a16_tc(const LinearArgs& a, cudaStream_t s, int* rc) {
   // NVFP4 weights, bf16 activations, one dense output; rows of whole 64-element chunks
   if (a.fmt != WQ_NVFP4 || a.M <= 16 || a.K % kKC != 0 || a.K < kKC) return 0;
   if (a.M > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF || ((uintptr_t)a.x & 15u) != 0) return 0;
-  // with fewer tiles than SMs the persistent kernel's choice of tile (128 rows for long K) spreads
-  // the work wider (1280 x 5120 at M = 1500: 469 against 380 TFLOP/s)
-  const int64_t items = ((a.N + kRows - 1) / kRows) * ((a.M + kHalf - 1) / kHalf);
-  if (items < num_sms_w16()) return 0;
-  *rc = launch_w4a16<1>(a, s);
-  return 1;
+  const int64_t ntiles = (a.N + kRows - 1) / kRows;
+  if (ntiles * ((a.M + 255) / 256) >= num_sms_w16()) {
+    *rc = launch_w4a16<256>(a, s);
+    return 1;
+  }
+  // fewer 256-row tiles than SMs: 128-row tiles, where they give most SMs an item
+  if (a.M >= kMinM128 && a.K <= kMaxK128 && ntiles * ((a.M + 127) / 128) >= kMinItems128) {
+    *rc = launch_w4a16<128>(a, s);
+    return 1;
+  }
+  return 0;
 }
 
 int take_status_w4a16() {

@@ -210,18 +210,21 @@ def test_w4a4_static_weights_flag(M, N, K):
 
 
 WIDE_W4A16 = [(2600, 4000, 320), (1100, 20000, 64), (5000, 2000, 1024), (2600, 20000, 128)]
+# fewer 256-row tiles than SMs: the same kernel with 128-row activation tiles (fc2 at one window;
+# ragged M and N with three chunks; one chunk)
+W4A16_128 = [(1500, 1280, 5120), (1000, 1480, 192), (777, 2000, 64)]
 
 
-@pytest.mark.parametrize("M,N,K", WIDE_W4A16)
+@pytest.mark.parametrize("M,N,K", WIDE_W4A16 + W4A16_128)
 def test_w4a16_wide_tiles(M, N, K):
     """NVFP4 W4A16 GEMMs on the kernel that decodes each weight tile into shared memory and
-    double-buffers its 256-row accumulators in TMEM: ragged M and N, one to sixteen 64-element chunks;
-    guard rows, tolerance, and bf16 output = fp32 output rounded once."""
+    double-buffers its 256- or 128-row accumulators in TMEM: ragged M and N, one to eighty 64-element
+    chunks; guard rows, tolerance, and bf16 output = fp32 output rounded once."""
     need_gpu()
     run_case("nvfp4", M, N, K, seed=M + N + K)
 
 
-@pytest.mark.parametrize("M,N,K", WIDE_W4A16)
+@pytest.mark.parametrize("M,N,K", WIDE_W4A16 + W4A16_128)
 def test_w4a16_wide_tiles_exact_products(M, N, K):
     """e2m1 * e4m3 weights are exact in bf16 and bf16 * bf16 products exact in fp32, so the fp32
     output differs from the fp64 oracle only by the accumulation order, the global-scale product and
