@@ -216,17 +216,32 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // pairs, without tables in memory.  The 3-bit magnitude of a code indexes the 8 bytes of two
 // registers in one byte permute: the high and the low bytes of the bf16 values of
 // {0, .5, 1, 1.5, 2, 3, 4, 6} are 00 3F 3F 3F 40 40 40 40 and 00 00 80 C0 00 40 80 C0.  The sign
-// bit of each code is replicated into bit 15 / 31 with prmt's sign-replicating selectors.
+// bits of four codes at a time go into the msbs of their high bytes before the bytes are paired: a
+// sign-replicating selector picks, for high byte k, the byte of u or of u << 4 whose msb is code k's
+// sign (u << 4 moves each low nibble's sign bit to its byte's msb).  X2P120: every value times 2^120
+// (high bytes 00 7B 7B 7B 7C 7C 7C 7C), the partner of e4m3_bf16pair_m120.
+template <bool X2P120 = false>
 __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t u, uint32_t (&w)[4]) {
-  constexpr uint32_t H0 = 0x3F3F3F00u, H1 = 0x40404040u, L0 = 0xC0800000u, L1 = 0xC0804000u;
+  constexpr uint32_t H0 = X2P120 ? 0x7B7B7B00u : 0x3F3F3F00u, H1 = X2P120 ? 0x7C7C7C7Cu : 0x40404040u;
+  constexpr uint32_t L0 = 0xC0800000u, L1 = 0xC0804000u;
   const uint32_t sa = u & 0x7777u, sb = (u >> 16) & 0x7777u;
-  const uint32_t hiA = prmt(H0, H1, sa), loA = prmt(L0, L1, sa);
-  const uint32_t hiB = prmt(H0, H1, sb), loB = prmt(L0, L1, sb);
-  const uint32_t u4 = u << 4;  // moves each low nibble's sign bit to its byte's msb
-  w[0] = prmt(loA, hiA, 0x5140u) | (prmt(u, u4, 0x80C0u) & 0x80008000u);
-  w[1] = prmt(loA, hiA, 0x7362u) | (prmt(u, u4, 0x90D0u) & 0x80008000u);
-  w[2] = prmt(loB, hiB, 0x5140u) | (prmt(u, u4, 0xA0E0u) & 0x80008000u);
-  w[3] = prmt(loB, hiB, 0x7362u) | (prmt(u, u4, 0xB0F0u) & 0x80008000u);
+  const uint32_t u4 = u << 4;
+  const uint32_t hiA = prmt(H0, H1, sa) | (prmt(u, u4, 0x9D8Cu) & 0x80808080u);  // codes 0..3
+  const uint32_t hiB = prmt(H0, H1, sb) | (prmt(u, u4, 0xBFAEu) & 0x80808080u);  // codes 4..7
+  const uint32_t loA = prmt(L0, L1, sa), loB = prmt(L0, L1, sb);
+  w[0] = prmt(loA, hiA, 0x5140u);
+  w[1] = prmt(loA, hiA, 0x7362u);
+  w[2] = prmt(loB, hiB, 0x5140u);
+  w[3] = prmt(loB, hiB, 0x7362u);
+}
+
+// x: an E4M3 code in bits 0..7 and again in bits 16..23 (zeros elsewhere).  Returns, in both bf16
+// halves, the code's value times 2^-120: its sign, exponent and mantissa fields moved to bf16's places
+// (exponent field e, mantissa m << 4).  Exact for every code, the subnormal codes landing on bf16
+// subnormals with the same mantissa; times an E2M1 value scaled by 2^120 the bf16 product is the
+// exact e2m1 * e4m3 (at most 5 significant bits, within bf16's normal range).
+__device__ __forceinline__ uint32_t e4m3_bf16pair_m120(uint32_t x) {
+  return ((x << 4) & 0x07F007F0u) | ((x << 8) & 0x80008000u);
 }
 
 // NVFP4: decode NE elements of one 64-element block with E2M1 -> bf16 in registers and the
@@ -240,10 +255,9 @@ __device__ __forceinline__ void decode_span_nvfp4_reg(uint32_t sword, int part, 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e0 = part * NE + q * 32 + j * 8;
-      const uint32_t sb = __float_as_uint(e4m3_to_f32((sword >> (8 * (e0 / 16))) & 0xFFu)) >> 16;
-      const uint32_t spair = sb | (sb << 16);
+      const uint32_t spair = e4m3_bf16pair_m120(prmt(sword, 0u, 0x4040u + 0x0101u * (e0 / 16)));
       uint32_t w[4];
-      e2m1x8_to_bf16(u[j], w);
+      e2m1x8_to_bf16<true>(u[j], w);
 #pragma unroll
       for (int b = 0; b < 4; ++b) out[q * 16 + j * 4 + b] = hmul2_bf16(w[b], spair);
     }

@@ -280,17 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint2 wv = *reinterpret_cast<const uint2*>(wsrc);
           u[0] = wv.x; u[1] = wv.y;
         }
-        uint32_t sp[SPC];
+        uint32_t sp[SPC];  // scale i times 2^-120 in both bf16 halves (the codes decode times 2^120)
 #pragma unroll
-        for (int i = 0; i < SPC; ++i) {
-          const uint32_t sb = __float_as_uint(e4m3_to_f32((sc >> (8 * i)) & 0xFFu)) >> 16;
-          sp[i] = sb | (sb << 16);
-        }
+        for (int i = 0; i < SPC; ++i) sp[i] = tc::e4m3_bf16pair_m120(tc::prmt(sc, 0u, 0x4040u + 0x0101u * i));
         uint8_t* arow = smem + L::A_OFF + slot * L::AB + r * 128;
 #pragma unroll
         for (int j = 0; j < kEPT / 8; ++j) {  // 8 codes -> four bf16 pairs -> one 16-byte chunk
           uint32_t w[4];
-          tc::e2m1x8_to_bf16(u[j], w);
+          tc::e2m1x8_to_bf16<true>(u[j], w);
           const uint32_t spair = sp[j >> 1];
           const uint4 o = make_uint4(tc::hmul2_bf16(w[0], spair), tc::hmul2_bf16(w[1], spair),
                                      tc::hmul2_bf16(w[2], spair), tc::hmul2_bf16(w[3], spair));

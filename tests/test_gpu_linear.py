@@ -201,6 +201,49 @@ def test_fp8_every_code_exact_through_each_path(path):
         np.array_equal(got, want)
 
 
+# (path, M): one activation row (CUDA-core GEMV), 16 rows grouped (tensor-core decode), 300 rows
+# (persistent GEMM), 1500 and 2600 rows (the W4A16 kernel's 128- and 256-row tiles at N = 2048)
+NVFP4_CODE_PATHS = [("gemv", 1), ("grouped_decode", 16), ("gemm", 300), ("gemm", 1500), ("gemm", 2600)]
+
+
+@pytest.mark.parametrize("path,M", NVFP4_CODE_PATHS)
+def test_nvfp4_every_code_and_scale_exact_through_each_path(path, M):
+    """Every E2M1 code (both signs) under every finite E4M3 block scale (0x01 .. 0x7E, the subnormal
+    scales included, plus zero blocks) with g = 1: block b of a row holds the eight E2M1 magnitudes
+    and their negatives times S_b = e4m3(b + 1), and the block holding 6 * 448 = 2688 sets g = 1, so
+    the packed scale codes are exactly b + 1 and each decoded weight is exactly e2m1 * S_b.  One-hot
+    activation rows pick single weights: every output must equal the oracle's decoded weight bit
+    for bit on every decode route."""
+    need_gpu()
+    mags = F.E2M1_MAGNITUDES.astype(np.float32)
+    S = F.e4m3_decode(np.arange(1, 0x7F)).astype(np.float32)          # 126 finite positive scales
+    blocks = np.concatenate([mags, -mags])[None, :] * S[:, None]       # [126, 16]
+    K, N = 2048, 2048
+    row = np.zeros(K, np.float32)
+    row[:blocks.size] = blocks.reshape(-1)                             # two zero blocks at the end
+    W = np.stack([np.roll(row, 16 * n) for n in range(N)]).astype(np.float32)
+    p_ref = oracle_pack("nvfp4", W)
+    assert p_ref["g"] == np.float32(1)
+    assert np.array_equal(p_ref["scales"].reshape(N, K // 16)[0, :126], np.arange(1, 0x7F))
+    w_hat = Q.nvfp4_dequant(p_ref)
+    ks = (np.arange(M) * 37) % K
+    x = np.zeros((M, K), np.float32)
+    x[np.arange(M), ks] = 1.0
+    xb = wl.to_bf16(x).cuda()
+    packed, scales = gpu_pack("nvfp4", W)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    if path == "grouped_decode":
+        wq().linear_grouped([(y, xb, packed, scales, N, K, None)], "nvfp4", out_f32=True)
+    else:
+        wq().linear_into(y, xb, packed, scales, "nvfp4", N, K, None, out_f32=True)
+    torch.cuda.synchronize()
+    assert wq().last_device_status() == 0
+    want = w_hat[:, ks].T.astype(np.float32)
+    got = y.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32) & 0x7FFFFFFF, want.view(np.uint32) & 0x7FFFFFFF) and \
+        np.array_equal(got, want)
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 1280, 1280), (1500, 5120, 1280), (130, 1280, 5120)])
 def test_w4a4_static_weights_flag(M, N, K):
     """W4A4 launched with programmatic dependent launch right after the activation quantiser: its
