@@ -18,9 +18,9 @@
 // Persistent CTA per SM over (weight tile, activation tile) items, warp-specialised:
 //   warp 0       TMA: activation tiles [BM x 64] (a stage is released by the MMAs reading it)
 //   warp 1       TMEM owner, MMA issuer (4 K steps per 64-element chunk)
-//   warps 2..17  dequant, two groups of eight taking alternate chunks (two chunks decode at once):
-//                E2M1 -> bf16 x E4M3 block scale, 32 elements of one row per thread, written
-//                swizzled into the shared-memory A ring
+//   warps 2..17  dequant, four groups of four each taking every fourth chunk (four chunks decode at
+//                once, each group in its own A slot): E2M1 -> bf16 x E4M3 block scale, a whole
+//                64-element row chunk per thread, written swizzled into the shared-memory A ring
 //   warps 18..21 epilogue: tcgen05.ld, * g, + bias, bf16 y through a 4 KB staging slab
 //   warp 22      TMA: weight codes [128 x 32 B] on a ring of their own, released by the dequant
 //                warps, so the decode runs ahead of the MMAs by up to the A ring's depth
@@ -42,8 +42,8 @@ namespace {
 constexpr int kRows = 128;       // weight rows per tile (MMA M)
 constexpr int kKC = 64;          // K elements per chunk: one 128-byte row of bf16
 constexpr int kNA = 4;           // decoded weight (A) slots (fills shared memory: 222 KB)
-constexpr int kDeqWarps = 16;                  // two groups of eight, alternate chunks
-constexpr int kDeqGroups = 2;
+constexpr int kDeqWarps = 16;                  // four groups of four, every fourth chunk
+constexpr int kDeqGroups = 4;
 constexpr int kGroupWarps = kDeqWarps / kDeqGroups;
 constexpr int kParts = kGroupWarps / 4;        // parts of a 64-element chunk
 constexpr int kEPT = kKC / kParts;             // elements a dequant thread decodes per chunk
@@ -51,7 +51,7 @@ constexpr int kEpiGroups = 1;                  // groups of four epilogue warps
 constexpr int kEpiWarp0 = 2 + kDeqWarps;
 constexpr int kWProdWarp = kEpiWarp0 + 4 * kEpiGroups;  // weight-code TMA
 constexpr int kThreads = (kWProdWarp + 1) * 32;
-static_assert(kEPT == 16 || kEPT == 32, "dequant part");
+static_assert(kEPT == 16 || kEPT == 32 || kEPT == 64, "dequant part");
 
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -237,10 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kEpiWarp0) {
     // ---------------------------------------------- dequant warps
-    // Group dg = (w - 2) / 8 decodes the chunks g with g % 2 == dg (every stage and slot index is even
-    // or odd with g, so each group has its own half of both rings); within it, warp w decodes rows
-    // 32 q + lane (q = (w - 2) % 4) and part pt = ((w - 2) / 4) % 2 of the chunk: kEPT / 2 code bytes
-    // and kEPT / 16 E4M3 scales, kEPT bf16 values of the row's 64.
+    // Group dg = (w - 2) / 4 decodes the chunks g with g % 4 == dg (the stage and slot indices follow
+    // g modulo multiples of 4, so each group has its own share of both rings); within it, warp w
+    // decodes rows 32 q + lane (q = (w - 2) % 4): kEPT / 2 code bytes and kEPT / 16 E4M3 scales per
+    // row and chunk, kEPT bf16 values of the row's 64.
     static_assert(kNA % kDeqGroups == 0 && L::WSTAGES % kDeqGroups == 0, "rings split between the groups");
     const int dw = warp - 2;
     const int dg = dw / kGroupWarps, q = dw & 3, pt = (dw % kGroupWarps) >> 2;
@@ -256,9 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* srow = p.scales + (row_ok ? n : 0) * nb16 + pt * SPC;
       auto scale_bytes = [&](int c) -> uint32_t {  // this part's scales of chunk c
         if (!row_ok) return 0u;
-        return SPC == 2 ? (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(srow + 4 * c)) : (uint32_t)__ldg(srow + 4 * c);
+        return SPC == 4   ? __ldg(reinterpret_cast<const uint32_t*>(srow + 4 * c))
+               : SPC == 2 ? (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(srow + 4 * c))
+                          : (uint32_t)__ldg(srow + 4 * c);
       };
-      const int c0 = ((gb & 1) == dg) ? 0 : 1;  // this group's first chunk of the item
+      const int c0 = (dg - gb % kDeqGroups + kDeqGroups) % kDeqGroups;  // this group's first chunk of the item
       uint32_t sc_next = c0 < nch ? scale_bytes(c0) : 0u;
       for (int c = c0; c < nch; c += kDeqGroups) {
         const int g = gb + c;
@@ -273,7 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t off = (uint32_t)(r * 32 + (boff & ~15)) ^ ((uint32_t)((r >> 2) & 1) << 4);
         const uint8_t* wsrc = smem + L::W_OFF + ws * L::WB + off + (boff & 15);
         uint32_t u[kEPT / 8];
-        if constexpr (kEPT == 32) {
+        if constexpr (kEPT == 64) {  // the whole 32-byte row: both 16-byte pieces (swizzle: bit 4 ^= bit 7)
+          const uint8_t* wrow = smem + L::W_OFF + ws * L::WB + r * 32;
+          const uint32_t sw = (uint32_t)((r >> 2) & 1) << 4;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(wrow + (0u ^ sw));
+          const uint4 w1 = *reinterpret_cast<const uint4*>(wrow + (16u ^ sw));
+          u[0] = w0.x; u[1] = w0.y; u[2] = w0.z; u[3] = w0.w;
+          u[4] = w1.x; u[5] = w1.y; u[6] = w1.z; u[7] = w1.w;
+        } else if constexpr (kEPT == 32) {
           const uint4 wv = *reinterpret_cast<const uint4*>(wsrc);
           u[0] = wv.x; u[1] = wv.y; u[2] = wv.z; u[3] = wv.w;
         } else {
