@@ -18,8 +18,9 @@
 //               buffered across items so the epilogue of one item overlaps the
 //               main loop of the next.
 //   warps 2..9  dequant: two warps per TMEM lane quarter, one thread per weight
-//               row and half chunk, packed codes -> bf16 pairs -> tcgen05.st
-//               into a TMEM ring of 2 to 4 A slots.
+//               row and half chunk (fold mode: per whole chunk, the two warps of a
+//               quarter taking alternate chunks), packed codes -> bf16 pairs ->
+//               tcgen05.st into a TMEM ring of 2 to 4 A slots.
 //   warps 10..13 epilogue: tcgen05.ld, x global scale (NVFP4), + bias, store y.
 //   warp 14     scale stager: one item ahead, bulk-copies the tile's scale slice
 //               into shared memory (NF4: also the tile's second-level scales).
@@ -263,6 +264,11 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   // the partial-tile ring has two slots (g & 1) whatever the A ring's depth
   constexpr int kDeqQ = p_deq_q<MODE>();
   constexpr int kDeqWarps = 4 * kDeqQ;
+  // fold mode: the kDeqQ warps of a lane quarter take whole chunks in turn (kDeqG groups, chunk g to
+  // group g % kDeqG); else each decodes 1/kDeqQ of every chunk
+  constexpr int kDeqG = FOLD ? kDeqQ : 1;
+  constexpr int kDeqPart = kDeqQ / kDeqG;  // parts of a chunk
+  constexpr int kGroupWarps = kDeqWarps / kDeqG;
   constexpr int kEpiWarp0 = p_epi_warp0<MODE>();
   constexpr int SCALE_CONSUMERS = FOLD ? 4 : kDeqWarps;
   constexpr int NWARPS = p_warps<MODE>();
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   constexpr int NISSUE = FOLD ? 4 : 1;  // MMA issuers; fold mode: two per chunk
   constexpr int CHUNK_COMMITS = FOLD ? 2 : 1;
   constexpr int SUB = S::SUB;
-  constexpr int NE = KC / kDeqQ;  // elements of a row each dequant warp decodes per chunk
+  constexpr int NE = KC / kDeqPart;  // elements of a row each dequant warp decodes per chunk
   static_assert(NE == 32 || NE % 64 == 0, "a dequant warp decodes half a 64-block or whole blocks");
   constexpr uint32_t IDESC = idesc_bf16(kRows, BN);
   constexpr int WCHUNK = Fmt<FMT>::WB * SUB;  // packed bytes of one row per chunk
@@ -311,9 +317,9 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&xfull[i], 1);
-      mbar_init(&empty[i], CHUNK_COMMITS + kDeqWarps);
+      mbar_init(&empty[i], CHUNK_COMMITS + kGroupWarps);
     }
-    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kDeqWarps); mbar_init(&aempty[i], CHUNK_COMMITS); }
+    for (int i = 0; i < kNA; ++i) { mbar_init(&afull[i], kGroupWarps); mbar_init(&aempty[i], CHUNK_COMMITS); }
     mbar_init(done, NWARPS);
     mbar_init(drain, NISSUE);
     for (int i = 0; i < 2; ++i) {
@@ -463,7 +469,8 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------ dequant warps: half h of every chunk
     const int q = warp & 3;
-    const int h = (warp - 2) / 4;  // which 1/kDeqQ of the chunk
+    const int h = ((warp - 2) / 4) % kDeqPart;    // which 1/kDeqPart of the chunk
+    const int grp = ((warp - 2) / 4) / kDeqPart;  // chunks g with g % kDeqG == grp
     const int r = q * 32 + lane;
     const int lsel = (LUTREP > 1) ? (lane & (LUTREP - 1)) : 0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -483,6 +490,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
       const int64_t g0 = ((int64_t)ic.nt * kRows * nb) / 256;  // NF4: first s2 group of the tile
       const float off = (FMT == WQ_NF4 && !FOLD) ? s2s[kS2Max - 1] : 0.0f;
       for (int c = 0; c < nch; ++c, ++g) {
+        if (kDeqG > 1 && g % kDeqG != grp) continue;  // another group's chunk
         const int s = g % STAGES, slot = g % kNA;
         constexpr int NBW = (NE >= 64) ? NE / 64 : 1;  // 64-blocks (or half of one) this warp decodes
         uint32_t sword[NBW];
@@ -506,8 +514,8 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         const uint8_t* wstage = smem + S::W_OFF + s * S::WB;
         constexpr int NES = NE / NBW;                          // elements per decode call (32 or 64)
         constexpr int CPS = NES / (Fmt<FMT>::BYTE ? 16 : 32);  // 16-byte chunks per call
-        const int ck0 = h * (WCHUNK / (16 * kDeqQ));            // first 16-byte chunk of this warp's part
-#pragma unroll
+        const int ck0 = h * (WCHUNK / (16 * kDeqPart));         // first 16-byte chunk of this warp's part
+#pragma unroll (FOLD ? 1 : NBW)  // fold: one 64-block at a time (no register spills)
         for (int bb = 0; bb < NBW; ++bb) {
           uint32_t v[NES / 2];
           if constexpr (Fmt<FMT>::UNIT) {
