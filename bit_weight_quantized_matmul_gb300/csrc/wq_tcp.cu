@@ -18,8 +18,8 @@
 //               buffered across items so the epilogue of one item overlaps the
 //               main loop of the next.
 //   warps 2..9  dequant: two warps per TMEM lane quarter, one thread per weight
-//               row and half chunk (fold mode: per whole chunk, the two warps of a
-//               quarter taking alternate chunks), packed codes -> bf16 pairs ->
+//               row and half chunk (NF4 fold mode: per whole chunk, the two warps of
+//               a quarter taking alternate chunks), packed codes -> bf16 pairs ->
 //               tcgen05.st into a TMEM ring of 2 to 4 A slots.
 //   warps 10..13 epilogue: tcgen05.ld, x global scale (NVFP4), + bias, store y.
 //   warp 14     scale stager: one item ahead, bulk-copies the tile's scale slice
@@ -264,9 +264,10 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   // the partial-tile ring has two slots (g & 1) whatever the A ring's depth
   constexpr int kDeqQ = p_deq_q<MODE>();
   constexpr int kDeqWarps = 4 * kDeqQ;
-  // fold mode: the kDeqQ warps of a lane quarter take whole chunks in turn (kDeqG groups, chunk g to
-  // group g % kDeqG); else each decodes 1/kDeqQ of every chunk
-  constexpr int kDeqG = FOLD ? kDeqQ : 1;
+  // NF4 fold mode: the kDeqQ warps of a lane quarter take whole chunks in turn (kDeqG groups, chunk g
+  // to group g % kDeqG); else each decodes 1/kDeqQ of every chunk (q4_0 decode measured 11 % slower
+  // in turns)
+  constexpr int kDeqG = (FOLD && FMT == WQ_NF4) ? kDeqQ : 1;
   constexpr int kDeqPart = kDeqQ / kDeqG;  // parts of a chunk
   constexpr int kGroupWarps = kDeqWarps / kDeqG;
   constexpr int kEpiWarp0 = p_epi_warp0<MODE>();
@@ -469,8 +470,8 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------ dequant warps: half h of every chunk
     const int q = warp & 3;
-    const int h = ((warp - 2) / 4) % kDeqPart;    // which 1/kDeqPart of the chunk
-    const int grp = ((warp - 2) / 4) / kDeqPart;  // chunks g with g % kDeqG == grp
+    const int h = kDeqG > 1 ? 0 : (warp - 2) / 4;    // which 1/kDeqPart of the chunk
+    const int grp = kDeqG > 1 ? (warp - 2) / 4 : 0;  // chunks g with g % kDeqG == grp
     const int r = q * 32 + lane;
     const int lsel = (LUTREP > 1) ? (lane & (LUTREP - 1)) : 0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(p_warps<MODE>() * 32, 1)
         constexpr int NES = NE / NBW;                          // elements per decode call (32 or 64)
         constexpr int CPS = NES / (Fmt<FMT>::BYTE ? 16 : 32);  // 16-byte chunks per call
         const int ck0 = h * (WCHUNK / (16 * kDeqPart));         // first 16-byte chunk of this warp's part
-#pragma unroll (FOLD ? 1 : NBW)  // fold: one 64-block at a time (no register spills)
+#pragma unroll (kDeqG > 1 ? 1 : NBW)  // whole chunks: one 64-block at a time (no register spills)
         for (int bb = 0; bb < NBW; ++bb) {
           uint32_t v[NES / 2];
           if constexpr (Fmt<FMT>::UNIT) {
